@@ -1,0 +1,330 @@
+// api.cu -- the extern "C" boundary declared in include/qmm.h: argument
+// validation, the N-based dispatcher, TMA tensor-map construction and the
+// per-device status word.
+#include <atomic>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/qmm.h"
+#include "kernels.h"
+
+namespace {
+
+using namespace qmm;
+
+// One status word per device, a static device variable (no allocation).
+__device__ unsigned g_qmm_status_word;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned *g_status_ptr[kMaxDevices];
+int g_num_sms[kMaxDevices];
+std::atomic<uint64_t> g_wait_limit{1ull << 31};   // ~1 s at 2 GHz
+
+struct DevInfo {
+    unsigned *status;
+    int num_sms;
+};
+
+bool dev_info(DevInfo &out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_status_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_qmm_status_word) != cudaSuccess) return false;
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+        g_status_ptr[dev] = static_cast<unsigned *>(p);
+        g_num_sms[dev] = sms;
+    }
+    out.status = g_status_ptr[dev];
+    out.num_sms = g_num_sms[dev];
+    return true;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no
+// link-time dependency on the driver library).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+bool block_geom(int wt, int &E, int &B) {
+    switch (wt) {
+    case QMM_Q8_0: E = 32; B = 34; return true;
+    case QMM_Q4_0: E = 32; B = 18; return true;
+    case QMM_Q4_K: E = 256; B = 144; return true;
+    case QMM_Q6_K: E = 256; B = 210; return true;
+    default: return false;
+    }
+}
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+    const uintptr_t a0 = (uintptr_t)a, b0 = (uintptr_t)b;
+    return a0 < b0 + nb && b0 < a0 + na;
+}
+
+int env_int(const char *name, int dflt) {
+    const char *v = std::getenv(name);
+    if (!v || !*v) return dflt;
+    return std::atoi(v);
+}
+
+// Dispatcher settings, read once per process.
+struct Settings {
+    int gemv_max_n;   // QMM_GEMV_MAX_N: largest N qmm_matmul sends to the GEMV
+    int force;        // QMM_FORCE_PATH: 0 none, 1 gemv, 2 gemm
+    int gemm_bn;      // QMM_GEMM_BN: 0 = model-based choice
+};
+const Settings &settings() {
+    static Settings s = [] {
+        Settings t;
+        t.gemv_max_n = env_int("QMM_GEMV_MAX_N", QMM_GEMV_MAX_N);
+        if (t.gemv_max_n < 0) t.gemv_max_n = 0;
+        if (t.gemv_max_n > QMM_GEMV_MAX_N) t.gemv_max_n = QMM_GEMV_MAX_N;
+        const char *f = std::getenv("QMM_FORCE_PATH");
+        t.force = (f && !std::strcmp(f, "gemv")) ? 1 : (f && !std::strcmp(f, "gemm")) ? 2 : 0;
+        t.gemm_bn = env_int("QMM_GEMM_BN", 0);
+        if (t.gemm_bn != 64 && t.gemm_bn != 128 && t.gemm_bn != 256) t.gemm_bn = 0;
+        return t;
+    }();
+    return s;
+}
+
+// Common validation of W, M, K, X, N, Y.
+qmm_status validate(int wt, const void *W, size_t w_bytes, int64_t M, int64_t K, const void *X, int xt,
+                    int64_t N, const float *Y, int64_t max_n, int &E, int &B) {
+    if (!block_geom(wt, E, B)) return QMM_ERR_INVALID_ARG;
+    if (xt != QMM_X_F32 && xt != QMM_X_BF16) return QMM_ERR_INVALID_ARG;
+    if (!W || !X || !Y) return QMM_ERR_INVALID_ARG;
+    if (M < 1 || K < 1 || M > (1ll << 30) || K > (1ll << 24)) return QMM_ERR_INVALID_ARG;
+    if (N < 1 || N > max_n) return QMM_ERR_INVALID_ARG;
+    if (K % E) return QMM_ERR_INVALID_ARG;
+    const size_t need = (size_t)M * (size_t)(K / E) * (size_t)B;
+    if (w_bytes < need) return QMM_ERR_INVALID_ARG;
+    const size_t xs = xt == QMM_X_F32 ? 4 : 2;
+    if (((uintptr_t)X) % xs || ((uintptr_t)Y) % 4) return QMM_ERR_INVALID_ARG;
+    const size_t ybytes = (size_t)N * (size_t)M * 4;
+    if (overlaps(Y, ybytes, W, need) || overlaps(Y, ybytes, X, (size_t)N * (size_t)K * xs))
+        return QMM_ERR_INVALID_ARG;
+    return QMM_OK;
+}
+
+qmm_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QMM_OK : QMM_ERR_CUDA; }
+
+int choose_bn(int64_t M, int64_t N, int num_sms) {
+    const int forced = settings().gemm_bn;
+    if (forced) return forced;
+    // Per 64-k stage a tile costs about max(dequant, MMA) cycles: the 128-row
+    // dequantization ~230 cycles, the MMA 2*BN cycles.  Pick the BN with the
+    // smallest (waves x stage time).
+    const int64_t tiles_m = (M + 127) / 128;
+    int best = 64;
+    double best_cost = 1e30;
+    for (int bn : {64, 128, 256}) {
+        if (bn > 64 && N <= bn / 2) continue;   // a smaller tile covers N
+        const int64_t tiles = tiles_m * ((N + bn - 1) / bn);
+        const int64_t waves = (tiles + num_sms - 1) / num_sms;
+        const double stage = bn * 2.0 > 230.0 ? bn * 2.0 : 230.0;
+        const double cost = (double)waves * stage * (bn == 256 ? 0.98 : 1.0);
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = bn;
+        }
+    }
+    return best;
+}
+
+qmm_status gemv_impl(int wt, const void *W, size_t w_bytes, int64_t M, int64_t K, const void *X, int xt, int64_t N,
+                     float *Y, void *stream) {
+    int E, B;
+    qmm_status s = validate(wt, W, w_bytes, M, K, X, xt, N, Y, QMM_GEMV_MAX_N, E, B);
+    if (s != QMM_OK) return s;
+    DevInfo di;
+    if (!dev_info(di)) return QMM_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int64_t row_bytes = K / E * B;
+    const bool aligned = ((uintptr_t)W % 16 == 0) && (row_bytes % 16 == 0) &&
+                         ((uintptr_t)X % 16 == 0) && ((K * (xt == QMM_X_F32 ? 4 : 2)) % 16 == 0);
+    if (aligned) {
+        cudaError_t e = launch_gemv_fast(wt, static_cast<const uint8_t *>(W), M, K, X, xt == QMM_X_BF16, (int)N,
+                                         Y, di.num_sms, st);
+        if (e != cudaErrorNotSupported) return from_cuda(e);
+        (void)cudaGetLastError();
+    }
+    return from_cuda(
+        launch_gemv_generic(wt, static_cast<const uint8_t *>(W), M, K, X, xt == QMM_X_BF16, (int)N, Y, st));
+}
+
+qmm_status gemm_impl(int wt, const void *W, size_t w_bytes, int64_t M, int64_t K, const void *X, int xt, int64_t N,
+                     float *Y, void *workspace, size_t ws_bytes, void *stream) {
+    int E, B;
+    qmm_status s = validate(wt, W, w_bytes, M, K, X, xt, N, Y, QMM_GEMM_MAX_N, E, B);
+    if (s != QMM_OK) return s;
+    const size_t ws_need = qmm_gemm_workspace_bytes(N, K, (qmm_xtype)xt);
+    if (ws_need && (!workspace || ws_bytes < ws_need || ((uintptr_t)workspace % 16))) return QMM_ERR_INVALID_ARG;
+    if (ws_need && (overlaps(workspace, ws_need, Y, (size_t)N * M * 4) ||
+                    overlaps(workspace, ws_need, X, (size_t)N * K * 4) ||
+                    overlaps(workspace, ws_need, W, (size_t)M * (K / E) * B)))
+        return QMM_ERR_INVALID_ARG;
+    // Tensor-core path geometry: 256-weight chunks, 16-byte aligned rows and
+    // bases for the TMA descriptors.
+    const int64_t row_bytes = K / E * B;
+    if (K % 256 || row_bytes % 16 || (uintptr_t)W % 16 || (uintptr_t)X % 16) return QMM_ERR_UNSUPPORTED;
+    if (M > (1ll << 31) - 1 || row_bytes / 2 > (1ll << 31)) return QMM_ERR_UNSUPPORTED;
+    DevInfo di;
+    if (!dev_info(di)) return QMM_ERR_CUDA;
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return QMM_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    const void *xb = X;
+    if (xt == QMM_X_F32) {
+        cudaError_t e = launch_x_to_bf16(static_cast<const float *>(X), N * K, static_cast<uint16_t *>(workspace), st);
+        if (e != cudaSuccess) return QMM_ERR_CUDA;
+        xb = workspace;
+    }
+    const int bn = choose_bn(M, N, di.num_sms);
+
+    CUtensorMap wmap, xmap;
+    {
+        const int win = gemm_raw_window_bytes(wt);
+        cuuint64_t dims[2] = {(cuuint64_t)(row_bytes / 2), (cuuint64_t)M};
+        cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+        cuuint32_t box[2] = {(cuuint32_t)(win / 2), 128u};
+        cuuint32_t estr[2] = {1u, 1u};
+        if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void *>(W), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return QMM_ERR_CUDA;
+    }
+    {
+        cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)N};
+        cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+        cuuint32_t box[2] = {64u, (cuuint32_t)bn};
+        cuuint32_t estr[2] = {1u, 1u};
+        if (enc(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(xb), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return QMM_ERR_CUDA;
+    }
+    GemmArgs a;
+    a.fmt = wt;
+    a.M = M;
+    a.K = K;
+    a.N = (int)N;
+    a.bn = bn;
+    a.Y = Y;
+    a.status = di.status;
+    a.wait_limit = g_wait_limit.load();
+    return from_cuda(launch_gemm_tc(a, wmap, xmap, st));
+}
+
+}  // namespace
+
+extern "C" {
+
+qmm_status qmm_block_info(qmm_wtype wt, int *elems, int *bytes) {
+    int E, B;
+    if (!block_geom(wt, E, B)) return QMM_ERR_INVALID_ARG;
+    if (elems) *elems = E;
+    if (bytes) *bytes = B;
+    return QMM_OK;
+}
+
+const char *qmm_status_str(qmm_status s) {
+    switch (s) {
+    case QMM_OK: return "QMM_OK";
+    case QMM_ERR_INVALID_ARG: return "QMM_ERR_INVALID_ARG";
+    case QMM_ERR_UNSUPPORTED: return "QMM_ERR_UNSUPPORTED";
+    case QMM_ERR_CUDA: return "QMM_ERR_CUDA";
+    case QMM_ERR_TIMEOUT: return "QMM_ERR_TIMEOUT";
+    default: return "QMM_UNKNOWN_STATUS";
+    }
+}
+
+size_t qmm_gemm_workspace_bytes(int64_t N, int64_t K, qmm_xtype xt) {
+    if (xt != QMM_X_F32 || N < 1 || K < 1) return 0;
+    return (size_t)N * (size_t)K * 2;
+}
+
+qmm_status qmm_gemv(qmm_wtype wt, const void *W, size_t w_bytes, int64_t M, int64_t K, const void *X, qmm_xtype xt,
+                    int64_t N, float *Y, void *stream) {
+    return gemv_impl(wt, W, w_bytes, M, K, X, xt, N, Y, stream);
+}
+
+qmm_status qmm_gemm(qmm_wtype wt, const void *W, size_t w_bytes, int64_t M, int64_t K, const void *X, qmm_xtype xt,
+                    int64_t N, float *Y, void *workspace, size_t ws_bytes, void *stream) {
+    return gemm_impl(wt, W, w_bytes, M, K, X, xt, N, Y, workspace, ws_bytes, stream);
+}
+
+qmm_status qmm_matmul(qmm_wtype wt, const void *W, size_t w_bytes, int64_t M, int64_t K, const void *X,
+                      qmm_xtype xt, int64_t N, float *Y, void *workspace, size_t ws_bytes, void *stream) {
+    const Settings &cfg = settings();
+    bool use_gemv = N <= cfg.gemv_max_n;
+    if (cfg.force == 1) use_gemv = N <= QMM_GEMV_MAX_N;
+    if (cfg.force == 2) use_gemv = false;
+    if (use_gemv) return gemv_impl(wt, W, w_bytes, M, K, X, xt, N, Y, stream);
+    return gemm_impl(wt, W, w_bytes, M, K, X, xt, N, Y, workspace, ws_bytes, stream);
+}
+
+qmm_status qmm_matmul_host(qmm_wtype wt, const void *W, size_t w_bytes, int64_t M, int64_t K, const void *X_host,
+                           qmm_xtype xt, int64_t N, float *Y_host, void *x_dev, float *y_dev, void *workspace,
+                           size_t ws_bytes, void *stream) {
+    if (!X_host || !Y_host || !x_dev || !y_dev) return QMM_ERR_INVALID_ARG;
+    if (N < 1 || N > QMM_GEMM_MAX_N || M < 1 || K < 1) return QMM_ERR_INVALID_ARG;
+    if (xt != QMM_X_F32 && xt != QMM_X_BF16) return QMM_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t xbytes = (size_t)N * (size_t)K * (xt == QMM_X_F32 ? 4 : 2);
+    const size_t ybytes = (size_t)N * (size_t)M * 4;
+    if (cudaMemcpyAsync(x_dev, X_host, xbytes, cudaMemcpyHostToDevice, st) != cudaSuccess) return QMM_ERR_CUDA;
+    qmm_status s = qmm_matmul(wt, W, w_bytes, M, K, x_dev, xt, N, y_dev, workspace, ws_bytes, stream);
+    if (s != QMM_OK) return s;
+    if (cudaMemcpyAsync(Y_host, y_dev, ybytes, cudaMemcpyDeviceToHost, st) != cudaSuccess) return QMM_ERR_CUDA;
+    return QMM_OK;
+}
+
+qmm_status qmm_dequant(qmm_wtype wt, const void *W, size_t w_bytes, int64_t M, int64_t K, float *out,
+                       void *stream) {
+    int E, B;
+    if (!block_geom(wt, E, B)) return QMM_ERR_INVALID_ARG;
+    if (!W || !out || M < 1 || K < 1 || K % E || M > (1ll << 30) || K > (1ll << 24)) return QMM_ERR_INVALID_ARG;
+    const size_t need = (size_t)M * (size_t)(K / E) * (size_t)B;
+    if (w_bytes < need || ((uintptr_t)out % 16)) return QMM_ERR_INVALID_ARG;
+    if (overlaps(out, (size_t)M * K * 4, W, need)) return QMM_ERR_INVALID_ARG;
+    return from_cuda(launch_dequant(wt, static_cast<const uint8_t *>(W), M, K, out, static_cast<cudaStream_t>(stream)));
+}
+
+qmm_status qmm_last_device_error(void *stream) {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return QMM_ERR_CUDA;
+    DevInfo di;
+    if (!dev_info(di)) return QMM_ERR_CUDA;
+    unsigned v = 0, zero = 0;
+    if (cudaMemcpy(&v, di.status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return QMM_ERR_CUDA;
+    if (v && cudaMemcpy(di.status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return QMM_ERR_CUDA;
+    return v == 0 ? QMM_OK : (qmm_status)v;
+}
+
+void qmm_set_wait_limit(uint64_t cycles) {
+    if (cycles < 1) cycles = 1;
+    if (cycles > (1ull << 40)) cycles = 1ull << 40;
+    g_wait_limit.store(cycles);
+}
+
+}  // extern "C"

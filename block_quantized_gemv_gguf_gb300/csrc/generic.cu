@@ -1,0 +1,130 @@
+// generic.cu -- byte-addressed kernels that accept any alignment:
+//   * dequant      : W -> f32 [M,K] (the bit-exact decoder check)
+//   * gemv_generic : Y[N,M] = X[N,K] W^T for 1 <= N <= 16, one warp per row
+//   * x_to_bf16    : f32 -> bf16 (round to nearest even) for the GEMM input
+#include "decode_bytes.cuh"
+#include "kernels.h"
+
+namespace qmm {
+
+template <int F>
+__global__ void __launch_bounds__(256) dequant_kernel(const uint8_t *__restrict__ W, int64_t M, int64_t K,
+                                                      float *__restrict__ out) {
+    const int64_t units_per_row = K / 32;
+    const int64_t total = M * units_per_row;
+    const int64_t row_bytes = K / Blk<F>::E * Blk<F>::B;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t m = i / units_per_row, u = i % units_per_row;
+        float w[32];
+        decode_unit<F>(W + m * row_bytes, u, w);
+        float4 *o = reinterpret_cast<float4 *>(out + m * K + u * 32);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] = make_float4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+    }
+}
+
+template <int F, bool XBF16>
+__global__ void __launch_bounds__(256) gemv_generic_kernel(const uint8_t *__restrict__ W, int64_t M, int64_t K,
+                                                           const void *__restrict__ Xv, int N,
+                                                           float *__restrict__ Y) {
+    const int lane = threadIdx.x & 31;
+    const int64_t m = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (m >= M) return;
+    const int64_t row_bytes = K / Blk<F>::E * Blk<F>::B;
+    const uint8_t *row = W + m * row_bytes;
+    float acc[16];
+#pragma unroll
+    for (int n = 0; n < 16; ++n) acc[n] = 0.f;
+    for (int64_t u = lane; u < K / 32; u += 32) {
+        float w[32];
+        decode_unit<F>(row, u, w);
+#pragma unroll
+        for (int n = 0; n < 16; ++n) {
+            if (n < N) {
+                float s = 0.f;
+                if constexpr (XBF16) {
+                    const __nv_bfloat16 *x = reinterpret_cast<const __nv_bfloat16 *>(Xv) + n * K + u * 32;
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) s = fmaf(w[e], __bfloat162float(x[e]), s);
+                } else {
+                    const float *x = reinterpret_cast<const float *>(Xv) + n * K + u * 32;
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) s = fmaf(w[e], __ldg(x + e), s);
+                }
+                acc[n] += s;
+            }
+        }
+    }
+#pragma unroll
+    for (int n = 0; n < 16; ++n) {
+        if (n < N) {
+            float v = acc[n];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            if (lane == 0) Y[(int64_t)n * M + m] = v;
+        }
+    }
+}
+
+__global__ void x_to_bf16_kernel(const float *__restrict__ X, int64_t count, __nv_bfloat16 *__restrict__ out) {
+    const int64_t i4 = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) * 4;
+    if (i4 + 3 < count && (reinterpret_cast<uintptr_t>(X) & 15) == 0) {
+        const float4 v = *reinterpret_cast<const float4 *>(X + i4);
+        out[i4] = __float2bfloat16_rn(v.x);
+        out[i4 + 1] = __float2bfloat16_rn(v.y);
+        out[i4 + 2] = __float2bfloat16_rn(v.z);
+        out[i4 + 3] = __float2bfloat16_rn(v.w);
+    } else {
+        for (int64_t i = i4; i < count && i < i4 + 4; ++i) out[i] = __float2bfloat16_rn(X[i]);
+    }
+}
+
+static int grid_for(int64_t work, int per_block) {
+    int64_t g = (work + per_block - 1) / per_block;
+    if (g > (1 << 20)) g = 1 << 20;
+    return (int)(g < 1 ? 1 : g);
+}
+
+cudaError_t launch_dequant(int fmt, const uint8_t *W, int64_t M, int64_t K, float *out, cudaStream_t st) {
+    const int g = grid_for(M * (K / 32), 256);
+    switch (fmt) {
+    case Q8_0: dequant_kernel<Q8_0><<<g, 256, 0, st>>>(W, M, K, out); break;
+    case Q4_0: dequant_kernel<Q4_0><<<g, 256, 0, st>>>(W, M, K, out); break;
+    case Q4_K: dequant_kernel<Q4_K><<<g, 256, 0, st>>>(W, M, K, out); break;
+    case Q6_K: dequant_kernel<Q6_K><<<g, 256, 0, st>>>(W, M, K, out); break;
+    default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+template <int F>
+static void gemv_generic_dispatch(const uint8_t *W, int64_t M, int64_t K, const void *X, int xbf16, int N,
+                                  float *Y, cudaStream_t st) {
+    const int g = (int)((M + 7) / 8);
+    if (xbf16)
+        gemv_generic_kernel<F, true><<<g, 256, 0, st>>>(W, M, K, X, N, Y);
+    else
+        gemv_generic_kernel<F, false><<<g, 256, 0, st>>>(W, M, K, X, N, Y);
+}
+
+cudaError_t launch_gemv_generic(int fmt, const uint8_t *W, int64_t M, int64_t K, const void *X, int xbf16,
+                                int N, float *Y, cudaStream_t st) {
+    switch (fmt) {
+    case Q8_0: gemv_generic_dispatch<Q8_0>(W, M, K, X, xbf16, N, Y, st); break;
+    case Q4_0: gemv_generic_dispatch<Q4_0>(W, M, K, X, xbf16, N, Y, st); break;
+    case Q4_K: gemv_generic_dispatch<Q4_K>(W, M, K, X, xbf16, N, Y, st); break;
+    case Q6_K: gemv_generic_dispatch<Q6_K>(W, M, K, X, xbf16, N, Y, st); break;
+    default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_x_to_bf16(const float *X, int64_t count, uint16_t *out, cudaStream_t st) {
+    if (count <= 0) return cudaSuccess;
+    const int g = grid_for((count + 3) / 4, 256);
+    x_to_bf16_kernel<<<g, 256, 0, st>>>(X, count, reinterpret_cast<__nv_bfloat16 *>(out));
+    return cudaGetLastError();
+}
+
+}  // namespace qmm

@@ -1,0 +1,212 @@
+"""Thin ctypes binding of the C ABI in include/qmm.h.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library (``_build/libqmm_gb300.so``).  There is no CPU fallback; if the
+library has not been built, every call raises.
+
+The ``qmm_*`` functions mirror the C entry points one to one (same names,
+same argument order; tensors stand in for device pointers, ``stream`` defaults
+to torch's current stream) and return the integer ``qmm_status``.  The short
+names (``gemv``, ``gemm``, ``matmul``, ``dequant``) allocate the output and
+raise ``QmmError`` on any non-OK status.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+Q8_0, Q4_0, Q4_K, Q6_K = 0, 1, 2, 3
+X_F32, X_BF16 = 0, 1
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = 0, 1, 2, 3, 4
+GEMV_MAX_N, GEMM_MAX_N = 16, 512
+BLOCK = {Q8_0: (32, 34), Q4_0: (32, 18), Q4_K: (256, 144), Q6_K: (256, 210)}
+EXPORTS = ("qmm_gemv", "qmm_gemm", "qmm_gemm_workspace_bytes", "qmm_matmul", "qmm_matmul_host",
+           "qmm_dequant", "qmm_block_info", "qmm_last_device_error", "qmm_status_str",
+           "qmm_set_wait_limit")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class QmmError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {status_name(status)}" if what else status_name(status))
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load() -> ctypes.CDLL:
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_build.LIB):
+            raise RuntimeError(f"CUDA library not built ({_build.LIB}); run __graft_entry__.build()")
+        lib = ctypes.CDLL(_build.LIB)
+        i64, sz, p, ci = ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_int
+        lib.qmm_gemv.argtypes = [ci, p, sz, i64, i64, p, ci, i64, p, p]
+        lib.qmm_gemm.argtypes = [ci, p, sz, i64, i64, p, ci, i64, p, p, sz, p]
+        lib.qmm_matmul.argtypes = [ci, p, sz, i64, i64, p, ci, i64, p, p, sz, p]
+        lib.qmm_matmul_host.argtypes = [ci, p, sz, i64, i64, p, ci, i64, p, p, p, p, sz, p]
+        lib.qmm_dequant.argtypes = [ci, p, sz, i64, i64, p, p]
+        lib.qmm_block_info.argtypes = [ci, p, p]
+        lib.qmm_last_device_error.argtypes = [p]
+        lib.qmm_gemm_workspace_bytes.argtypes = [i64, i64, ci]
+        lib.qmm_gemm_workspace_bytes.restype = sz
+        lib.qmm_status_str.argtypes = [ci]
+        lib.qmm_status_str.restype = ctypes.c_char_p
+        lib.qmm_set_wait_limit.argtypes = [ctypes.c_uint64]
+        lib.qmm_set_wait_limit.restype = None
+        for f in ("qmm_gemv", "qmm_gemm", "qmm_matmul", "qmm_matmul_host", "qmm_dequant", "qmm_block_info",
+                  "qmm_last_device_error"):
+            getattr(lib, f).restype = ci
+        _lib = lib
+        return lib
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return stream
+
+
+def _xtype(X) -> int:
+    if X.dtype == torch.float32:
+        return X_F32
+    if X.dtype == torch.bfloat16:
+        return X_BF16
+    raise TypeError("X must be float32 or bfloat16")
+
+
+def _nbytes(t) -> int:
+    return t.numel() * t.element_size()
+
+
+def status_name(s: int) -> str:
+    return load().qmm_status_str(s).decode()
+
+
+# --------------------------------------------------------------------------
+# one-to-one mirrors of the C entry points (return qmm_status)
+# --------------------------------------------------------------------------
+def qmm_gemv(wt, W, M, K, X, N, Y, stream=None, w_bytes=None, xt=None) -> int:
+    return load().qmm_gemv(wt, _ptr(W), _nbytes(W) if w_bytes is None else w_bytes, M, K, _ptr(X),
+                           _xtype(X) if xt is None else xt, N, _ptr(Y), _stream(stream))
+
+
+def qmm_gemm(wt, W, M, K, X, N, Y, workspace=None, ws_bytes=None, stream=None, w_bytes=None, xt=None) -> int:
+    if ws_bytes is None:
+        ws_bytes = 0 if workspace is None else _nbytes(workspace)
+    return load().qmm_gemm(wt, _ptr(W), _nbytes(W) if w_bytes is None else w_bytes, M, K, _ptr(X),
+                           _xtype(X) if xt is None else xt, N, _ptr(Y), _ptr(workspace), ws_bytes,
+                           _stream(stream))
+
+
+def qmm_matmul(wt, W, M, K, X, N, Y, workspace=None, ws_bytes=None, stream=None, w_bytes=None, xt=None) -> int:
+    if ws_bytes is None:
+        ws_bytes = 0 if workspace is None else _nbytes(workspace)
+    return load().qmm_matmul(wt, _ptr(W), _nbytes(W) if w_bytes is None else w_bytes, M, K, _ptr(X),
+                             _xtype(X) if xt is None else xt, N, _ptr(Y), _ptr(workspace), ws_bytes,
+                             _stream(stream))
+
+
+def qmm_matmul_host(wt, W, M, K, X_host, N, Y_host, x_dev, y_dev, workspace=None, ws_bytes=None,
+                    stream=None) -> int:
+    if ws_bytes is None:
+        ws_bytes = 0 if workspace is None else _nbytes(workspace)
+    return load().qmm_matmul_host(wt, _ptr(W), _nbytes(W), M, K, _ptr(X_host), _xtype(X_host), N, _ptr(Y_host),
+                                  _ptr(x_dev), _ptr(y_dev), _ptr(workspace), ws_bytes, _stream(stream))
+
+
+def qmm_dequant(wt, W, M, K, out, stream=None, w_bytes=None) -> int:
+    return load().qmm_dequant(wt, _ptr(W), _nbytes(W) if w_bytes is None else w_bytes, M, K, _ptr(out),
+                              _stream(stream))
+
+
+def qmm_block_info(wt):
+    e, b = ctypes.c_int(), ctypes.c_int()
+    s = load().qmm_block_info(wt, ctypes.byref(e), ctypes.byref(b))
+    return s, e.value, b.value
+
+
+def qmm_gemm_workspace_bytes(N, K, xt) -> int:
+    return load().qmm_gemm_workspace_bytes(N, K, xt)
+
+
+def qmm_last_device_error(stream=None) -> int:
+    return load().qmm_last_device_error(_stream(stream))
+
+
+def qmm_status_str(s: int) -> str:
+    return status_name(s)
+
+
+def qmm_set_wait_limit(cycles: int) -> None:
+    load().qmm_set_wait_limit(cycles)
+
+
+# --------------------------------------------------------------------------
+# convenience wrappers (allocate the output, raise on error)
+# --------------------------------------------------------------------------
+def _check(s: int, what: str):
+    if s != OK:
+        raise QmmError(s, what)
+
+
+def _shape(X, K):
+    if X.dim() != 2 or X.shape[1] != K:
+        raise ValueError(f"X must be [N, {K}]")
+    return X.shape[0]
+
+
+def gemv(wt, W, M, K, X, Y=None, stream=None):
+    N = _shape(X, K)
+    Y = torch.empty((N, M), dtype=torch.float32, device=X.device) if Y is None else Y
+    _check(qmm_gemv(wt, W, M, K, X, N, Y, stream), "qmm_gemv")
+    return Y
+
+
+def workspace_for(N, K, X):
+    n = qmm_gemm_workspace_bytes(N, K, _xtype(X))
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=X.device) if n else None
+
+
+def gemm(wt, W, M, K, X, Y=None, workspace=None, stream=None):
+    N = _shape(X, K)
+    Y = torch.empty((N, M), dtype=torch.float32, device=X.device) if Y is None else Y
+    workspace = workspace_for(N, K, X) if workspace is None else workspace
+    _check(qmm_gemm(wt, W, M, K, X, N, Y, workspace, stream=stream), "qmm_gemm")
+    return Y
+
+
+def matmul(wt, W, M, K, X, Y=None, workspace=None, stream=None):
+    N = _shape(X, K)
+    Y = torch.empty((N, M), dtype=torch.float32, device=X.device) if Y is None else Y
+    workspace = workspace_for(N, K, X) if workspace is None else workspace
+    _check(qmm_matmul(wt, W, M, K, X, N, Y, workspace, stream=stream), "qmm_matmul")
+    return Y
+
+
+def dequant(wt, W, M, K, out=None, stream=None):
+    out = torch.empty((M, K), dtype=torch.float32, device=W.device) if out is None else out
+    _check(qmm_dequant(wt, W, M, K, out, stream), "qmm_dequant")
+    return out

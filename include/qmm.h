@@ -1,0 +1,185 @@
+/*
+ * qmm.h -- C ABI of the GB300 (sm_103a) block-quantized projection matmul.
+ *
+ *     Y[n, m] = sum_k  X[n, k] * w(m, k)        0 <= n < N, 0 <= m < M
+ *
+ * W[M, K] is stored in GGUF/ggml block-quantized layouts and dequantized on
+ * the fly inside the kernels.  This is the projection matmul of the dense
+ * transformer in "cera 0.5.0 src/model/llama.rs" (per-token decode GEMV,
+ * project_logits / project_logits_batched for the LM head,
+ * forward_prefill_batched for the batched prefill GEMM) whose scalar
+ * definition is matmul_q4_0_f32 / matmul_q8_0_f32 / matmul_q4km_f32 and the
+ * gemv_* row loops of "cera 0.5.2 src/backend/cpu.rs".
+ *
+ * Layouts (all little endian, blocks stored back to back):
+ *   W      row m is K / E_blk consecutive blocks; rows are consecutive, so
+ *          row m starts at byte m * (K / E_blk) * B_blk ("cera 0.5.2
+ *          src/backend/cpu.rs" matmul_*_f32).
+ *   Q8_0   34 B / 32 weights: f16 d @0, int8 q[32] @2; w = d * q.
+ *   Q4_0   18 B / 32 weights: f16 d @0, qs[16] @2; weight e < 16 is the low
+ *          nibble of qs[e], weight e >= 16 the high nibble of qs[e-16];
+ *          w = (nibble - 8) * d ("cera 0.5.2 src/backend/cpu.rs",
+ *          repack_q4_0_8x8).
+ *   Q4_K   144 B / 256 weights: f16 d @0, f16 dmin @2, 12 packed scale bytes
+ *          @4, qs[128] @16.  Sub-block s = e / 32 uses the low (s even) or
+ *          high (s odd) nibble of qs[(s/2)*32 + e%32]; six-bit (sc_s, m_s)
+ *          are packed in GGUF order; w = d*sc_s*q - dmin*m_s ("cera 0.5.2
+ *          src/backend/cpu.rs", repack_q4_k_8x8).
+ *   Q6_K   210 B / 256 weights: ql[128] @0, qh[64] @128, int8 scales[16]
+ *          @192, f16 d @208; weight e = 128h + 32j + l takes its low four
+ *          bits from ql[64h + 32(j%2) + l] (low nibble for j < 2, high for
+ *          j >= 2) and bits 2j..2j+1 of qh[32h + l] as bits 4..5;
+ *          w = d * scales[e/16] * (q - 32) (GGUF layout; the 210-byte size is
+ *          "cera 0.3.1 src/model/gpu_lfm2.rs", weight upload).
+ *   X      [N, K] row-major, f32 or bf16, device memory.
+ *   Y      [N, M] row-major f32, device memory, OVERWRITTEN (not accumulated,
+ *          as the scalar row loops assign their sum).
+ *
+ * Conventions common to every call:
+ *   - All pointers are device pointers unless the name says host.  The
+ *     caller owns every buffer; the library allocates nothing per call.  The
+ *     only allocation is one small device status word per device, made on the
+ *     first call on that device.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Every call is asynchronous and stream ordered; there is no
+ *     hidden global state, so calls on different streams may run
+ *     concurrently on disjoint outputs.
+ *   - Arguments are validated on the host before anything is launched; on a
+ *     validation error nothing is written and no kernel runs.  The checks
+ *     mirror the release asserts of "cera 0.5.2 src/backend/cpu.rs"
+ *     gemm_preq_dispatch (K a multiple of the block size, enough weight
+ *     bytes for M rows) turned into status codes, plus: pointers non-null,
+ *     M, K >= 1, N within the call's range, Y not overlapping W or X.
+ *   - An unknown format is QMM_ERR_INVALID_ARG (the pages' GEMV dispatcher
+ *     panics on it); a supported format on a path that cannot take the given
+ *     shape or alignment is QMM_ERR_UNSUPPORTED, never a silent fallback
+ *     (the pages warn that a silent per-token fallback cost ~4x prefill;
+ *     "cera 0.5.0 src/model/llama.rs", forward_prefill_batched).
+ *   - Device-side waits are bounded.  A kernel that gives up records
+ *     QMM_ERR_TIMEOUT in the device status word; qmm_last_device_error
+ *     reports and clears it.
+ */
+#ifndef QMM_H
+#define QMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define QMM_API __attribute__((visibility("default")))
+#else
+#define QMM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { QMM_Q8_0 = 0, QMM_Q4_0 = 1, QMM_Q4_K = 2, QMM_Q6_K = 3 } qmm_wtype;
+typedef enum { QMM_X_F32 = 0, QMM_X_BF16 = 1 } qmm_xtype;
+typedef enum {
+    QMM_OK = 0,
+    QMM_ERR_INVALID_ARG = 1,
+    QMM_ERR_UNSUPPORTED = 2,
+    QMM_ERR_CUDA = 3,
+    QMM_ERR_TIMEOUT = 4
+} qmm_status;
+
+/* Largest N per call of each path.  512 is the batched-prefill chunk
+ * ("cera 0.3.1 src/model/gpu_lfm2.rs", MAX_PREFILL_TOKENS). */
+#define QMM_GEMV_MAX_N 16
+#define QMM_GEMM_MAX_N 512
+
+/*
+ * Multi-token GEMV, 1 <= N <= QMM_GEMV_MAX_N: decode (N = 1) and small-N
+ * batches such as speculative verification through the LM head
+ * ("cera 0.5.0 src/model/llama.rs", project_logits and
+ * project_logits_batched).  Every weight block is read from HBM once and
+ * reused for all N tokens; arithmetic is f32 on the exact dequantized
+ * weights (|error| <= 1e-5 * sum|w x| + 1e-6 against exact arithmetic).
+ *   W        raw blocks, w_bytes >= M * (K / E_blk) * B_blk.  Any alignment;
+ *            the fast path needs W 16-byte aligned and a row size that is a
+ *            multiple of 16 bytes, otherwise a byte-addressed path runs.
+ *   X        [N, K] f32 or bf16 (xt), 4-byte (f32) / 2-byte (bf16) aligned.
+ *   Y        [N, M] f32, 4-byte aligned, overwritten.
+ */
+QMM_API qmm_status qmm_gemv(qmm_wtype wt, const void *W, size_t w_bytes, int64_t M, int64_t K,
+                    const void *X, qmm_xtype xt, int64_t N, float *Y, void *stream);
+
+/*
+ * Prefill GEMM on the tensor cores, 1 <= N <= QMM_GEMM_MAX_N
+ * ("cera 0.5.0 src/model/llama.rs", forward_prefill_batched and its
+ * per-layer projection GEMMs; "cera 0.3.1 src/model/gpu_lfm2.rs",
+ * build_mul_mat_pipeline: weights are dequantized once per K tile in shared
+ * memory and reused across all token columns).  Weight tiles are staged by
+ * TMA, dequantized to bf16 in shared memory and multiplied by tcgen05 MMA
+ * with f32 accumulation in tensor memory (|error| <= 2e-3 * sum|w x| + 1e-5).
+ * Requirements (else QMM_ERR_UNSUPPORTED): K % 256 == 0 (K % 2048 == 0 for
+ * Q6_K), W and X 16-byte aligned.
+ *   workspace  device scratch of at least qmm_gemm_workspace_bytes(N, K, xt)
+ *              bytes, 16-byte aligned (may be NULL when that size is 0):
+ *              f32 X is converted to bf16 there before the GEMM.
+ */
+QMM_API qmm_status qmm_gemm(qmm_wtype wt, const void *W, size_t w_bytes, int64_t M, int64_t K,
+                    const void *X, qmm_xtype xt, int64_t N, float *Y,
+                    void *workspace, size_t ws_bytes, void *stream);
+
+/* Bytes of workspace qmm_gemm / qmm_matmul need: N*K*2 for f32 X, else 0. */
+QMM_API size_t qmm_gemm_workspace_bytes(int64_t N, int64_t K, qmm_xtype xt);
+
+/*
+ * N-based dispatcher, 1 <= N <= QMM_GEMM_MAX_N: N <= QMM_GEMV_MAX_N runs
+ * qmm_gemv, larger N runs qmm_gemm.  Same arguments as qmm_gemm (the
+ * workspace is only touched on the GEMM path).
+ */
+QMM_API qmm_status qmm_matmul(qmm_wtype wt, const void *W, size_t w_bytes, int64_t M, int64_t K,
+                      const void *X, qmm_xtype xt, int64_t N, float *Y,
+                      void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * qmm_matmul with the per-step inputs and outputs in HOST memory:
+ * copies X_host -> x_dev, runs qmm_matmul, copies y_dev -> Y_host, all
+ * asynchronously on `stream` (pin the host buffers for overlap).  W stays
+ * resident in device memory.  x_dev (>= N*K*sizeof(x element) bytes) and
+ * y_dev (>= N*M*4 bytes) are caller-provided device staging buffers.  The
+ * host output is valid after the stream is synchronized.
+ */
+QMM_API qmm_status qmm_matmul_host(qmm_wtype wt, const void *W, size_t w_bytes, int64_t M, int64_t K,
+                           const void *X_host, qmm_xtype xt, int64_t N, float *Y_host,
+                           void *x_dev, float *y_dev,
+                           void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * Dequantize W[M, K] to f32 out[M, K] (row-major, device).  Every value is
+ * the exact dequantized weight rounded once to nearest-even f32 (exact for
+ * Q8_0, Q4_0 and Q6_K).  Used to check the block decoders bit for bit.
+ */
+QMM_API qmm_status qmm_dequant(qmm_wtype wt, const void *W, size_t w_bytes, int64_t M, int64_t K,
+                       float *out, void *stream);
+
+/* Weights and bytes per block of a format (Q8_0 32/34, Q4_0 32/18,
+ * Q4_K 256/144, Q6_K 256/210). */
+QMM_API qmm_status qmm_block_info(qmm_wtype wt, int *elems, int *bytes);
+
+/*
+ * Synchronizes `stream`, then returns and clears the current device's status
+ * word: QMM_OK, or QMM_ERR_TIMEOUT if a kernel gave up on a bounded wait
+ * since the last call, or QMM_ERR_CUDA if the stream reports an error.
+ */
+QMM_API qmm_status qmm_last_device_error(void *stream);
+
+/* Static, human-readable name of a status code. */
+QMM_API const char *qmm_status_str(qmm_status s);
+
+/*
+ * Test hook: upper bound, in SM clock cycles, on every device-side wait of
+ * the tensor-core GEMM (default about two seconds).  A tiny limit makes the
+ * waits give up, which tests use to exercise the QMM_ERR_TIMEOUT path
+ * without a hang.  Affects launches issued after the call, process wide.
+ */
+QMM_API void qmm_set_wait_limit(uint64_t cycles);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
