@@ -159,13 +159,26 @@ qmm_status gemv_impl(int wt, const void *W, size_t w_bytes, int64_t M, int64_t K
     if (!dev_info(di)) return QMM_ERR_CUDA;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int64_t row_bytes = K / E * B;
-    const bool aligned = ((uintptr_t)W % 16 == 0) && (row_bytes % 16 == 0) &&
-                         ((uintptr_t)X % 16 == 0) && ((K * (xt == QMM_X_F32 ? 4 : 2)) % 16 == 0);
-    if (aligned) {
-        cudaError_t e = launch_gemv_fast(wt, static_cast<const uint8_t *>(W), M, K, X, xt == QMM_X_BF16, (int)N,
-                                         Y, di.num_sms, st);
-        if (e != cudaErrorNotSupported) return from_cuda(e);
-        (void)cudaGetLastError();
+    // Tensor-core GEMV: whole 256-weight chunks, TMA-able rows (16-byte
+    // aligned base and row pitch), 16-byte aligned X.  Anything else takes the
+    // byte-addressed kernel, which computes the same sums.
+    const bool fast = K % 256 == 0 && row_bytes % 16 == 0 && (uintptr_t)W % 16 == 0 && (uintptr_t)X % 16 == 0 &&
+                      M <= (1ll << 31) - 1;
+    if (fast) {
+        EncodeTiledFn enc = encode_fn();
+        if (!enc) return QMM_ERR_CUDA;
+        CUtensorMap wmap;
+        const int win = gemv_window_bytes(wt);
+        cuuint64_t dims[2] = {(cuuint64_t)(row_bytes / 2), (cuuint64_t)M};
+        cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+        cuuint32_t box[2] = {(cuuint32_t)(win / 2), 64u};
+        cuuint32_t estr[2] = {1u, 1u};
+        if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void *>(W), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return QMM_ERR_CUDA;
+        return from_cuda(launch_gemv_mma(wt, wmap, X, xt == QMM_X_BF16, M, K, (int)N, Y, di.num_sms, di.status,
+                                         g_wait_limit.load(), st));
     }
     return from_cuda(
         launch_gemv_generic(wt, static_cast<const uint8_t *>(W), M, K, X, xt == QMM_X_BF16, (int)N, Y, st));

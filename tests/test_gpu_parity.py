@@ -137,7 +137,19 @@ def test_gemv_parity(wt, M, K, N):
 
 
 @pytest.mark.parametrize("wt", ALL, ids=IDS)
-@pytest.mark.parametrize("N", [1, 4, 16])
+@pytest.mark.parametrize("N", [1, 8, 16])
+def test_gemv_many_rows_no_k_split(wt, N):
+    """Enough row tiles that the GEMV runs without a K split (one CTA per tile)."""
+    M, K = 16000, 2048
+    w = synth.gen_weights(wt, M, K, "gemv-big")
+    x = synth.gen_x(N, K, "gemv-big")
+    y = run("gemv", wt, w, M, K, x)
+    rows = np.sort(np.random.default_rng(N).choice(M, 512, replace=False))
+    check(y, w, wt, M, K, x, GEMV_TOL, rows=rows)
+
+
+@pytest.mark.parametrize("wt", ALL, ids=IDS)
+@pytest.mark.parametrize("N", [1, 4, 9, 16])
 def test_gemv_bf16_x(wt, N):
     M, K = 257, 2048
     w = synth.gen_weights(wt, M, K, "gemv-bf16")
