@@ -124,6 +124,35 @@ QMM_API qmm_status qmm_gemm(qmm_wtype wt, const void *W, size_t w_bytes, int64_t
                     const void *X, qmm_xtype xt, int64_t N, float *Y,
                     void *workspace, size_t ws_bytes, void *stream);
 
+/*
+ * qmm_gemm without a workspace, for callers that may not allocate device
+ * memory: a plugin or custom operator whose host framework owns every byte of
+ * device memory and offers no scratch argument, a deployment with a fixed,
+ * pre-planned memory budget, or a latency-critical path that must avoid the
+ * device-wide synchronization cudaMalloc / cudaFree can cause.
+ * (The cera pages have no counterpart: their kernels run on CPU threads and
+ * reuse host Vec scratch, and the wgpu path allocates its buffers at load.)
+ *
+ * Same arguments and results as qmm_gemm.  When X is f32 the bf16 copy of X
+ * goes to a library-owned, statically sized device array of
+ * QMM_NOALLOC_SCRATCH_BYTES instead of a workspace; every GPU that loads the
+ * library holds that array until the process exits.  Nothing is allocated by
+ * this call.
+ *   - N*K*2 > QMM_NOALLOC_SCRATCH_BYTES (f32 X) returns QMM_ERR_UNSUPPORTED
+ *     and launches nothing; bf16 X needs no scratch and has no extra limit.
+ *   - The first call on a device looks up the array's device address for
+ *     that device (cudaGetSymbolAddress) and caches it; make that first call
+ *     before any stream capture.
+ *   - All calls share the one array.  Each call rewrites the part it uses
+ *     before reading it, so no clearing is needed, but calls whose kernels
+ *     overlap on the GPU (different streams, no ordering between them) race
+ *     on the array and give wrong results: order them on one stream or with
+ *     events.
+ */
+#define QMM_NOALLOC_SCRATCH_BYTES (16u << 20)
+QMM_API qmm_status qmm_gemm_noalloc(qmm_wtype wt, const void *W, size_t w_bytes, int64_t M, int64_t K,
+                                    const void *X, qmm_xtype xt, int64_t N, float *Y, void *stream);
+
 /* Bytes of workspace qmm_gemm / qmm_matmul need: N*K*2 for f32 X, else 0. */
 QMM_API size_t qmm_gemm_workspace_bytes(int64_t N, int64_t K, qmm_xtype xt);
 
