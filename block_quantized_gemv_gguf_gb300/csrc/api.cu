@@ -171,13 +171,23 @@ qmm_status gemv_impl(int wt, const void *W, size_t w_bytes, int64_t M, int64_t K
         const int win = gemv_window_bytes(wt);
         cuuint64_t dims[2] = {(cuuint64_t)(row_bytes / 2), (cuuint64_t)M};
         cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
-        cuuint32_t box[2] = {(cuuint32_t)(win / 2), 64u};
+        cuuint32_t box[2] = {(cuuint32_t)(win / 2), (cuuint32_t)gemv_tile_rows(M, di.num_sms)};
         cuuint32_t estr[2] = {1u, 1u};
         if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void *>(W), dims, strides, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return QMM_ERR_CUDA;
-        return from_cuda(launch_gemv_mma(wt, wmap, X, xt == QMM_X_BF16, M, K, (int)N, Y, di.num_sms, di.status,
+        CUtensorMap xmap;
+        const int xes = xt == QMM_X_F32 ? 4 : 2;
+        cuuint64_t xdims[2] = {(cuuint64_t)K, (cuuint64_t)N};
+        cuuint64_t xstrides[1] = {(cuuint64_t)K * xes};
+        cuuint32_t xbox[2] = {256u, (cuuint32_t)N};
+        if (enc(&xmap, xt == QMM_X_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                const_cast<void *>(X), xdims, xstrides, xbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return QMM_ERR_CUDA;
+        return from_cuda(launch_gemv_mma(wt, wmap, xmap, xt == QMM_X_BF16, M, K, (int)N, Y, di.num_sms, di.status,
                                          g_wait_limit.load(), st));
     }
     return from_cuda(

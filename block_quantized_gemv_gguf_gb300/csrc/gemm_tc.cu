@@ -254,8 +254,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     if (warp == WARP_WPROD) {
         if (lane == 0) {
-            int last[SR];
-            for (int r = 0; r < SR; ++r) last[r] = -1;
+            int issued = 0;   // raw chunks are issued in order 0, 1, ..., issued-1
             for (int c = 0; c < nkc; ++c) {
                 const int r = c % SR;
                 if (c >= SR && !wait_ok(ctl, &raw_empty[r], ((c / SR) - 1) & 1, wait_limit)) break;
@@ -267,27 +266,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     xb = c * RAWB;
                 mbar_arrive_expect_tx(&raw_full[r], (uint32_t)L::RAW_BYTES);
                 tma_load_2d(sRaw + r * L::RAW_BYTES, &wmap, &raw_full[r], xb >> 1, m0);
-                last[r] = c;
+                issued = c + 1;
             }
-            if (*abort_flag)
-                for (int r = 0; r < SR; ++r)
-                    if (last[r] >= 0) drain(&raw_full[r], (last[r] / SR) & 1, drain_limit);
+            if (*abort_flag)   // drain: the last load issued into each stage
+                for (int c = issued - SR < 0 ? 0 : issued - SR; c < issued; ++c)
+                    drain(&raw_full[c % SR], (c / SR) & 1, drain_limit);
         }
     } else if (warp == WARP_XPROD) {
         if (lane == 0) {
-            int last[SA];
-            for (int s = 0; s < SA; ++s) last[s] = -1;
+            int issued = 0;
             for (int t = 0; t < nsteps; ++t) {
                 const int s = t % SA;
                 if (t >= SA && !wait_ok(ctl, &ab_empty[s], ((t / SA) - 1) & 1, wait_limit)) break;
                 if (*abort_flag) break;
                 mbar_arrive_expect_tx(&x_full[s], (uint32_t)L::X_BYTES);
                 tma_load_2d(sX + s * L::X_BYTES, &xmap, &x_full[s], t * BK, n0);
-                last[s] = t;
+                issued = t + 1;
             }
             if (*abort_flag)
-                for (int s = 0; s < SA; ++s)
-                    if (last[s] >= 0) drain(&x_full[s], (last[s] / SA) & 1, drain_limit);
+                for (int t = issued - SA < 0 ? 0 : issued - SA; t < issued; ++t)
+                    drain(&x_full[t % SA], (t / SA) & 1, drain_limit);
         }
     } else if (warp == WARP_MMA) {
         if (lane == 0) {

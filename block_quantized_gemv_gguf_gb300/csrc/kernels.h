@@ -15,12 +15,17 @@ cudaError_t launch_gemv_generic(int fmt, const uint8_t *W, int64_t M, int64_t K,
                                 int N, float *Y, cudaStream_t st);
 
 // Tensor-core GEMV, 1 <= N <= 16 (K % 256 == 0, 16-byte aligned W rows and
-// X).  wmap: raw weight bytes as u16 [M][row_bytes/2], box {window/2, 64}.
-cudaError_t launch_gemv_mma(int fmt, const CUtensorMap &wmap, const void *X, int xbf16, int64_t M, int64_t K, int N,
-                            float *Y, int num_sms, unsigned *status, uint64_t limit, cudaStream_t st);
+// X).  wmap: raw weight bytes as u16 [M][row_bytes/2], box {window/2, 64};
+// xmap: X [N][K] (f32 or bf16), box {256, N}.
+cudaError_t launch_gemv_mma(int fmt, const CUtensorMap &wmap, const CUtensorMap &xmap, int xbf16, int64_t M,
+                            int64_t K, int N, float *Y, int num_sms, unsigned *status, uint64_t limit,
+                            cudaStream_t st);
 
 // Raw bytes of one 256-weight chunk of a row in the GEMV's staging.
 int gemv_window_bytes(int fmt);
+
+// Rows per GEMV tile (the weight tensor map's box height) for M rows.
+int gemv_tile_rows(int64_t M, int num_sms);
 
 // bf16 out[i] = round-to-nearest-even(X[i]).
 cudaError_t launch_x_to_bf16(const float *X, int64_t count, uint16_t *out, cudaStream_t st);

@@ -138,9 +138,11 @@ def test_gemv_parity(wt, M, K, N):
 
 @pytest.mark.parametrize("wt", ALL, ids=IDS)
 @pytest.mark.parametrize("N", [1, 8, 16])
-def test_gemv_many_rows_no_k_split(wt, N):
-    """Enough row tiles that the GEMV runs without a K split (one CTA per tile)."""
-    M, K = 16000, 2048
+@pytest.mark.parametrize("M", [16000, 40000])
+def test_gemv_many_rows_no_k_split(wt, N, M):
+    """Enough row tiles that the GEMV runs without a K split (one CTA per
+    tile); 40000 rows selects the 128-row tile variant on a 152-SM GPU."""
+    K = 2048
     w = synth.gen_weights(wt, M, K, "gemv-big")
     x = synth.gen_x(N, K, "gemv-big")
     y = run("gemv", wt, w, M, K, x)
