@@ -54,6 +54,30 @@ def peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+# DRAM bytes (read + write) per pass of an op, summed over its kernels, from
+# one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum), keyed by the
+# sha256 of the kernel sources they were taken on.  A source change since the
+# capture turns the figure into null.
+TRAFFIC = {}
+
+
+def _kernel_hash():
+    import hashlib
+    h = hashlib.sha256()
+    cs = os.path.join(ROOT, "block_quantized_gemv_gguf_gb300", "csrc")
+    for f in sorted(os.listdir(cs)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(cs, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(op):
+    t = TRAFFIC.get(op)
+    if not t or t[0] != _kernel_hash():
+        return None
+    return t[1]
+
+
 def wbytes(wt, M, K):
     return synth.weight_bytes(wt, M, K)
 
@@ -131,29 +155,23 @@ def run_gpu(args):
         dist.init_process_group("nccl")
     dev = torch.device("cuda", local)
     qmm.load()
+    # Weights are written once and then only read: let each call start
+    # streaming its weights before the preceding kernel on the stream ends.
+    qmm.qmm_set_static_weights(not args.no_static_weights)
     hbm_peak, bf16_peak, bf16_sus, peak_src = peaks()
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 126 * 1024 * 1024) or 126 * 1024 * 1024
     R = args.copies
 
+    only = set(args.only.split(",")) if args.only else {"decode", "lmhead", "prefill"}
+    bad = only - {"decode", "lmhead", "prefill"}
+    if bad:
+        raise SystemExit(f"unknown op(s) in --only: {sorted(bad)}")
+
     # ---- inputs: generated once on the host, replicated R times on device ----
     def make(wt, M, K, name):
         w = torch.from_numpy(synth.gen_weights(wt, M, K, name)).to(dev)
         return [w] + [w.clone() for _ in range(R - 1)]
-
-    dec_w = [make(synth.Q4_0, M, K, f"bench-decode-{M}x{K}") for (M, K) in DECODE_SHAPES]
-    dec_x = [torch.from_numpy(synth.gen_x(1, K, f"bench-decode-{K}")).to(dev) for (_, K) in DECODE_SHAPES]
-    dec_y = [torch.empty(1, M, device=dev) for (M, _) in DECODE_SHAPES]
-    Mh, Kh, Nh = LMHEAD
-    head_w = torch.from_numpy(synth.gen_weights(synth.Q6_K, Mh, Kh, "bench-lmhead")).to(dev)
-    head_x = torch.from_numpy(synth.gen_x(Nh, Kh, "bench-lmhead")).to(dev)
-    head_y = torch.empty(Nh, Mh, device=dev)
-    pre_w = [make(synth.Q4_K, M, K, f"bench-prefill-{M}x{K}") for (M, K) in PREFILL_SHAPES]
-    pre_x = [torch.from_numpy(synth.gen_x(PREFILL_N, K, f"bench-prefill-{K}")).to(dev) for (_, K) in PREFILL_SHAPES]
-    pre_y = [torch.empty(PREFILL_N, M, device=dev) for (M, _) in PREFILL_SHAPES]
-    pre_ws = [qmm.workspace_for(PREFILL_N, K, x) for x, (_, K) in zip(pre_x, PREFILL_SHAPES)]
-    rot_bytes = R * sum(wbytes(synth.Q4_0, M, K) for M, K in DECODE_SHAPES)
-    torch.cuda.synchronize()
 
     stream = torch.cuda.Stream(device=dev)
 
@@ -161,72 +179,102 @@ def run_gpu(args):
         if s != qmm.OK:
             raise RuntimeError(qmm.status_name(s))
 
-    def op_decode(r):
-        for i, (M, K) in enumerate(DECODE_SHAPES):
-            chk(qmm.qmm_matmul(synth.Q4_0, dec_w[i][r], M, K, dec_x[i], 1, dec_y[i], stream=stream))
+    ops, launches_per_pass = {}, {}
+    Mh, Kh, Nh = LMHEAD
+    if "decode" in only:
+        dec_w = [make(synth.Q4_0, M, K, f"bench-decode-{M}x{K}") for (M, K) in DECODE_SHAPES]
+        dec_x = [torch.from_numpy(synth.gen_x(1, K, f"bench-decode-{K}")).to(dev) for (_, K) in DECODE_SHAPES]
+        dec_y = [torch.empty(1, M, device=dev) for (M, _) in DECODE_SHAPES]
 
-    def op_lmhead(r):
-        chk(qmm.qmm_matmul(synth.Q6_K, head_w, Mh, Kh, head_x, Nh, head_y, stream=stream))
+        def op_decode(r):
+            for i, (M, K) in enumerate(DECODE_SHAPES):
+                chk(qmm.qmm_matmul(synth.Q4_0, dec_w[i][r], M, K, dec_x[i], 1, dec_y[i], stream=stream))
+        ops["decode"], launches_per_pass["decode"] = op_decode, len(DECODE_SHAPES)
+    if "lmhead" in only:
+        # one copy: 431 MB alone is more than three times L2
+        head_w = torch.from_numpy(synth.gen_weights(synth.Q6_K, Mh, Kh, "bench-lmhead")).to(dev)
+        head_x = torch.from_numpy(synth.gen_x(Nh, Kh, "bench-lmhead")).to(dev)
+        head_y = torch.empty(Nh, Mh, device=dev)
 
-    def op_prefill(r):
-        for i, (M, K) in enumerate(PREFILL_SHAPES):
-            chk(qmm.qmm_matmul(synth.Q4_K, pre_w[i][r], M, K, pre_x[i], PREFILL_N, pre_y[i], pre_ws[i],
-                               stream=stream))
+        def op_lmhead(r):
+            chk(qmm.qmm_matmul(synth.Q6_K, head_w, Mh, Kh, head_x, Nh, head_y, stream=stream))
+        ops["lmhead"], launches_per_pass["lmhead"] = op_lmhead, 1
+    if "prefill" in only:
+        pre_w = [make(synth.Q4_K, M, K, f"bench-prefill-{M}x{K}") for (M, K) in PREFILL_SHAPES]
+        pre_x = [torch.from_numpy(synth.gen_x(PREFILL_N, K, f"bench-prefill-{K}")).to(dev)
+                 for (_, K) in PREFILL_SHAPES]
+        pre_y = [torch.empty(PREFILL_N, M, device=dev) for (M, _) in PREFILL_SHAPES]
+        pre_ws = [qmm.workspace_for(PREFILL_N, K, x) for x, (_, K) in zip(pre_x, PREFILL_SHAPES)]
 
-    launches_per_pass = {"decode": len(DECODE_SHAPES), "lmhead": 1, "prefill": 2 * len(PREFILL_SHAPES)}
-    ops = {"decode": op_decode, "lmhead": op_lmhead, "prefill": op_prefill}
+        def op_prefill(r):
+            for i, (M, K) in enumerate(PREFILL_SHAPES):
+                chk(qmm.qmm_matmul(synth.Q4_K, pre_w[i][r], M, K, pre_x[i], PREFILL_N, pre_y[i], pre_ws[i],
+                                   stream=stream))
+        ops["prefill"], launches_per_pass["prefill"] = op_prefill, 2 * len(PREFILL_SHAPES)
+    rot_bytes = R * sum(wbytes(synth.Q4_0, M, K) for M, K in DECODE_SHAPES)
+    torch.cuda.synchronize()
 
-    # warm-up outside capture (also sets kernel attributes)
+    # warm-up outside capture (also sets kernel attributes): one pass per copy
     with torch.cuda.stream(stream):
         for r in range(R):
             for f in ops.values():
                 f(r)
     torch.cuda.synchronize()
 
-    graphs = {}
-    for name, f in ops.items():
+    # One CUDA graph per op over all R copies (step s uses copy s % R), plus
+    # one over the first K % R copies, so that exactly K steps are timed.
+    K_steps = max(1, args.steps)
+    full, rem = divmod(K_steps, R)
+
+    def capture(f, passes):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            for r in range(R):
+            for r in range(passes):
                 f(r)
-        graphs[name] = g
+        return g
+
+    graphs = {name: (capture(f, R), capture(f, rem) if rem else None) for name, f in ops.items()}
     torch.cuda.synchronize()
 
-    def time_graph(name, reps):
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    def replay(g):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
-            for a, b in ev:
-                a.record(stream)
-                graphs[name].replay()
-                b.record(stream)
-        stream.synchronize()
-        return [a.elapsed_time(b) / R for a, b in ev]    # ms per pass over one weight copy
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+        return a, b
 
-    for _ in range(max(args.warmup, 3)):
+    warm_replays = max(1, -(-max(args.warmup, 3) // R))
+    for _ in range(warm_replays):
         for name in graphs:
-            time_graph(name, 1)
+            replay(graphs[name][0])
+    torch.cuda.synchronize()
 
-    # ---- timed region: K steps; each step = one pass of every op ----
+    # ---- timed region: exactly K steps; each step = one pass of every op ----
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     clk = Clocks(local)
     clk.start()
     time.sleep(0.3)
-    reps = max(1, -(-args.steps // R))   # graph replays cover R steps each
-    per_op = {name: [] for name in graphs}
+    events = {name: [] for name in graphs}
     t0 = time.perf_counter()
-    for _ in range(reps):
+    for _ in range(full):
         for name in graphs:
-            per_op[name] += time_graph(name, 1)
+            events[name].append((replay(graphs[name][0]), R))
+    if rem:
+        for name in graphs:
+            events[name].append((replay(graphs[name][1]), rem))
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
     clocks = clk.stop()
     if world > 1:
         torch.distributed.barrier()
 
-    med = {k: statistics.median(v) for k, v in per_op.items()}           # ms per pass
-    steps_timed = reps * R
+    med = {}      # ms per pass (one step of that op), total event time / K
+    for name, evs in events.items():
+        med[name] = sum(a.elapsed_time(b) for (a, b), _ in evs) / K_steps
+    steps_timed = K_steps
     ms_step = sum(med.values())
     if world > 1:
         t = torch.tensor([ms_step], device=dev)
@@ -234,31 +282,31 @@ def run_gpu(args):
         ms_step = float(t.item())
 
     dec_bytes = sum(alg_bytes(synth.Q4_0, M, K, 1, 4) for M, K in DECODE_SHAPES)
-    decode_gbs = dec_bytes / (med["decode"] * 1e-3) / 1e9 * world
     head_bytes = alg_bytes(synth.Q6_K, Mh, Kh, Nh, 4)
-    head_gbs = head_bytes / (med["lmhead"] * 1e-3) / 1e9
     pre_flops = sum(2.0 * M * K * PREFILL_N for M, K in PREFILL_SHAPES)
-    pre_tflops = pre_flops / (med["prefill"] * 1e-3) / 1e12
+    decode_gbs = dec_bytes / (med["decode"] * 1e-3) / 1e9 * world if "decode" in med else None
+    head_gbs = head_bytes / (med["lmhead"] * 1e-3) / 1e9 if "lmhead" in med else None
+    pre_tflops = pre_flops / (med["prefill"] * 1e-3) / 1e12 if "prefill" in med else None
 
     # dominant kernel of the step -> roofline object
     shares = {k: v / sum(med.values()) for k, v in med.items()}
     dom = max(shares, key=shares.get)
     if dom == "prefill":
         roof = {"bound": "tensor", "achieved": round(pre_tflops, 1), "peak": bf16_peak, "unit": "TFLOP/s",
-                "frac": round(pre_tflops / bf16_peak, 4), "traffic": None, "kernel": "gemm_tc (Q4_K, N=512)",
-                "peak_source": f"bf16_tflops ({peak_src})"}
+                "frac": round(pre_tflops / bf16_peak, 4), "traffic": traffic_for("prefill"),
+                "kernel": "gemm_tc (Q4_K, N=512) + x_to_bf16", "peak_source": f"bf16_tflops ({peak_src})"}
     elif dom == "lmhead":
         roof = {"bound": "hbm", "achieved": round(head_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
-                "frac": round(head_gbs / hbm_peak, 4), "traffic": None, "kernel": "gemv (Q6_K, N=8)",
-                "peak_source": f"hbm_gbs ({peak_src})"}
+                "frac": round(head_gbs / hbm_peak, 4), "traffic": traffic_for("lmhead"),
+                "kernel": "gemv_mma (Q6_K 128256x4096, N=8)", "peak_source": f"hbm_gbs ({peak_src})"}
     else:
         roof = {"bound": "hbm", "achieved": round(decode_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
-                "frac": round(decode_gbs / hbm_peak, 4), "traffic": None, "kernel": "gemv (Q4_0, N=1)",
-                "peak_source": f"hbm_gbs ({peak_src})"}
+                "frac": round(decode_gbs / hbm_peak, 4), "traffic": traffic_for("decode"),
+                "kernel": "gemv_mma (Q4_0, N=1)", "peak_source": f"hbm_gbs ({peak_src})"}
 
     # ---- end to end: host X in, host Y out, through qmm_matmul_host ----
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and "decode" in ops:
         xh = [torch.from_numpy(synth.gen_x(1, K, f"bench-decode-{K}")).pin_memory() for (_, K) in DECODE_SHAPES]
         yh = [torch.empty(1, M).pin_memory() for (M, _) in DECODE_SHAPES]
         xd = [torch.empty(1, K, device=dev) for (_, K) in DECODE_SHAPES]
@@ -272,17 +320,10 @@ def run_gpu(args):
             for r in range(R):
                 e2e_pass(r)
         stream.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for r in range(R):
-                e2e_pass(r)
+        g = capture(e2e_pass, R)
         ts = []
-        for _ in range(max(3, reps)):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            with torch.cuda.stream(stream):
-                a.record(stream)
-                g.replay()
-                b.record(stream)
+        for _ in range(max(3, full)):
+            a, b = replay(g)
             stream.synchronize()
             ts.append(a.elapsed_time(b) / R)
         t_e2e = statistics.median(ts)
@@ -292,15 +333,13 @@ def run_gpu(args):
                "ms_per_step": round(t_e2e, 5),
                "path": "qmm_matmul_host (pinned host X -> device, GEMV, device Y -> pinned host)"}
 
-    cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(args.cpu_seconds)
-
     launches = steps_timed * sum(launches_per_pass.values())
+    r1 = lambda v, nd=1: None if v is None else round(v, nd)    # noqa: E731
+    value = decode_gbs if decode_gbs is not None else (head_gbs if head_gbs is not None else pre_tflops)
     line = {
         "metric": METRIC,
-        "value": round(decode_gbs, 1),
-        "unit": "GB/s",
+        "value": r1(value),
+        "unit": "GB/s" if (decode_gbs is not None or head_gbs is not None) else "TFLOP/s",
         "n_gpus": world,
         "steps": steps_timed,
         "warmup": max(args.warmup, 3),
@@ -310,27 +349,33 @@ def run_gpu(args):
         "vs_baseline": None,
         "dtype": "f32 (GEMV); bf16 x bf16 -> f32 (GEMM)",
         "data": "synthetic (seeded random blocks and N(0,1) activations)",
-        "config": {"workload": WORKLOAD, "decode_N": 1, "lmhead_N": Nh, "prefill_N": PREFILL_N,
-                   "weight_copies": R, "rotating_bytes": rot_bytes, "l2_bytes": l2,
+        "config": {"workload": WORKLOAD if len(ops) == 3 else f"subset: {sorted(ops)}",
+                   "decode_N": 1, "lmhead_N": Nh, "prefill_N": PREFILL_N,
+                   "weight_copies": R, "static_weights": not args.no_static_weights, "rotating_bytes": rot_bytes, "l2_bytes": l2,
                    "l2_policy": f"inputs larger than L2: {R} rotating weight copies ({rot_bytes / 2**20:.0f} MiB "
-                                f"for the decode shapes)"},
-        "decode": {"GBps": round(decode_gbs, 1), "frac_of_measured_hbm": round(decode_gbs / hbm_peak, 4),
-                   "frac_of_nominal_8TBps": round(decode_gbs / NOMINAL_HBM_GBS, 4),
-                   "us_per_pass": round(med["decode"] * 1e3, 3),
-                   "per_shape_bytes": [alg_bytes(synth.Q4_0, M, K, 1, 4) for M, K in DECODE_SHAPES]},
-        "lmhead": {"GBps": round(head_gbs, 1), "frac_of_measured_hbm": round(head_gbs / hbm_peak, 4),
-                   "us": round(med["lmhead"] * 1e3, 3), "N": Nh},
-        "prefill": {"TFLOPs": round(pre_tflops, 1), "frac_of_measured_bf16": round(pre_tflops / bf16_peak, 4),
-                    "us": round(med["prefill"] * 1e3, 3), "N": PREFILL_N,
-                    "includes": "f32->bf16 conversion of X + tensor-core GEMM"},
+                                f"for the decode shapes); the 431 MB LM head alone exceeds L2"},
         "step_share": {k: round(v, 4) for k, v in shares.items()},
         "roofline": roof,
-        "cpu_baseline": cpu,
+        "cpu_baseline": None,
         "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clocks,
         "wall_s_timed": round(wall, 3),
     }
+    if decode_gbs is not None:
+        line["decode"] = {"GBps": r1(decode_gbs), "frac_of_measured_hbm": round(decode_gbs / hbm_peak, 4),
+                          "frac_of_nominal_8TBps": round(decode_gbs / NOMINAL_HBM_GBS, 4),
+                          "us_per_pass": round(med["decode"] * 1e3, 3),
+                          "per_shape_bytes": [alg_bytes(synth.Q4_0, M, K, 1, 4) for M, K in DECODE_SHAPES]}
+    if head_gbs is not None:
+        line["lmhead"] = {"GBps": r1(head_gbs), "frac_of_measured_hbm": round(head_gbs / hbm_peak, 4),
+                          "us": round(med["lmhead"] * 1e3, 3), "N": Nh}
+    if pre_tflops is not None:
+        line["prefill"] = {"TFLOPs": r1(pre_tflops), "frac_of_measured_bf16": round(pre_tflops / bf16_peak, 4),
+                           "us": round(med["prefill"] * 1e3, 3), "N": PREFILL_N,
+                           "includes": "f32->bf16 conversion of X + tensor-core GEMM"}
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line))
     if world > 1:
@@ -414,6 +459,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-static-weights", action="store_true",
+                    help="launch every call only after the preceding kernel has finished")
+    ap.add_argument("--only", default="", help="comma list of ops to run (decode,lmhead,prefill); default all")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

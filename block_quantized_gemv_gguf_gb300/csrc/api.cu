@@ -21,6 +21,22 @@ std::mutex g_mu;
 unsigned *g_status_ptr[kMaxDevices];
 int g_num_sms[kMaxDevices];
 std::atomic<uint64_t> g_wait_limit{1ull << 31};   // ~1 s at 2 GHz
+// Static-weights mode (programmatic dependent launch): -1 = not set through
+// the API, take QMM_STATIC_WEIGHTS from the environment.
+std::atomic<int> g_static_weights{-1};
+// Set while qmm_matmul_host runs its compute call: that call follows a
+// host-to-device copy, not a kernel, so it is launched the ordinary way.
+thread_local bool t_after_copy = false;
+bool static_weights() {
+    if (t_after_copy) return false;
+    const int v = g_static_weights.load();
+    if (v >= 0) return v != 0;
+    static const bool env = [] {
+        const char *e = std::getenv("QMM_STATIC_WEIGHTS");
+        return e && std::atoi(e) != 0;
+    }();
+    return env;
+}
 
 struct DevInfo {
     unsigned *status;
@@ -90,6 +106,10 @@ struct Settings {
     int gemv_max_n;   // QMM_GEMV_MAX_N: largest N qmm_matmul sends to the GEMV
     int force;        // QMM_FORCE_PATH: 0 none, 1 gemv, 2 gemm
     int gemm_bn;      // QMM_GEMM_BN: 0 = model-based choice
+    int gemv_rows;    // QMM_GEMV_ROWS: 64, 128 or 256 rows per GEMV tile; 0 = by M
+    int gemv_rg;      // QMM_GEMV_RG: 16-row groups per warp (1 or 2) of the resident-X GEMV
+    int gemv_ks;      // QMM_GEMV_KS: K split of the GEMV (1..8); 0 = automatic
+    int gemv_res;     // QMM_GEMV_RESIDENT: 0 disables the resident-X GEMV
 };
 const Settings &settings() {
     static Settings s = [] {
@@ -101,6 +121,12 @@ const Settings &settings() {
         t.force = (f && !std::strcmp(f, "gemv")) ? 1 : (f && !std::strcmp(f, "gemm")) ? 2 : 0;
         t.gemm_bn = env_int("QMM_GEMM_BN", 0);
         if (t.gemm_bn != 64 && t.gemm_bn != 128 && t.gemm_bn != 256) t.gemm_bn = 0;
+        t.gemv_rows = env_int("QMM_GEMV_ROWS", 0);
+        if (t.gemv_rows != 64 && t.gemv_rows != 128 && t.gemv_rows != 256) t.gemv_rows = 0;
+        t.gemv_rg = env_int("QMM_GEMV_RG", 0) == 2 ? 2 : 1;
+        t.gemv_ks = env_int("QMM_GEMV_KS", 0);
+        if (t.gemv_ks < 0 || t.gemv_ks > 8) t.gemv_ks = 0;
+        t.gemv_res = env_int("QMM_GEMV_RESIDENT", 1) != 0;
         return t;
     }();
     return s;
@@ -167,11 +193,14 @@ qmm_status gemv_impl(int wt, const void *W, size_t w_bytes, int64_t M, int64_t K
     if (fast) {
         EncodeTiledFn enc = encode_fn();
         if (!enc) return QMM_ERR_CUDA;
+        const Settings &cfg = settings();
+        const GemvTuning tun{cfg.gemv_rows, cfg.gemv_rg, cfg.gemv_ks, cfg.gemv_res};
+        const GemvPlan plan = plan_gemv(M, K, (int)N, xt == QMM_X_BF16, di.num_sms, tun);
         CUtensorMap wmap;
         const int win = gemv_window_bytes(wt);
         cuuint64_t dims[2] = {(cuuint64_t)(row_bytes / 2), (cuuint64_t)M};
         cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
-        cuuint32_t box[2] = {(cuuint32_t)(win / 2), (cuuint32_t)gemv_tile_rows(M, di.num_sms)};
+        cuuint32_t box[2] = {(cuuint32_t)(win / 2), (cuuint32_t)plan.rows};
         cuuint32_t estr[2] = {1u, 1u};
         if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void *>(W), dims, strides, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -187,8 +216,8 @@ qmm_status gemv_impl(int wt, const void *W, size_t w_bytes, int64_t M, int64_t K
                 CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return QMM_ERR_CUDA;
-        return from_cuda(launch_gemv_mma(wt, wmap, xmap, xt == QMM_X_BF16, M, K, (int)N, Y, di.num_sms, di.status,
-                                         g_wait_limit.load(), st));
+        return from_cuda(launch_gemv_mma(wt, plan, wmap, xmap, X, xt == QMM_X_BF16, M, K, (int)N, Y,
+                                         static_weights(), di.status, g_wait_limit.load(), st));
     }
     return from_cuda(
         launch_gemv_generic(wt, static_cast<const uint8_t *>(W), M, K, X, xt == QMM_X_BF16, (int)N, Y, st));
@@ -218,7 +247,8 @@ qmm_status gemm_impl(int wt, const void *W, size_t w_bytes, int64_t M, int64_t K
 
     const void *xb = X;
     if (xt == QMM_X_F32) {
-        cudaError_t e = launch_x_to_bf16(static_cast<const float *>(X), N * K, static_cast<uint16_t *>(workspace), st);
+        cudaError_t e = launch_x_to_bf16(static_cast<const float *>(X), N * K, static_cast<uint16_t *>(workspace),
+                                         static_weights(), st);
         if (e != cudaSuccess) return QMM_ERR_CUDA;
         xb = workspace;
     }
@@ -255,6 +285,7 @@ qmm_status gemm_impl(int wt, const void *W, size_t w_bytes, int64_t M, int64_t K
     a.Y = Y;
     a.status = di.status;
     a.wait_limit = g_wait_limit.load();
+    a.pdl = static_weights() ? 1 : 0;
     return from_cuda(launch_gemm_tc(a, wmap, xmap, st));
 }
 
@@ -316,7 +347,9 @@ qmm_status qmm_matmul_host(qmm_wtype wt, const void *W, size_t w_bytes, int64_t 
     const size_t xbytes = (size_t)N * (size_t)K * (xt == QMM_X_F32 ? 4 : 2);
     const size_t ybytes = (size_t)N * (size_t)M * 4;
     if (cudaMemcpyAsync(x_dev, X_host, xbytes, cudaMemcpyHostToDevice, st) != cudaSuccess) return QMM_ERR_CUDA;
+    t_after_copy = true;
     qmm_status s = qmm_matmul(wt, W, w_bytes, M, K, x_dev, xt, N, y_dev, workspace, ws_bytes, stream);
+    t_after_copy = false;
     if (s != QMM_OK) return s;
     if (cudaMemcpyAsync(Y_host, y_dev, ybytes, cudaMemcpyDeviceToHost, st) != cudaSuccess) return QMM_ERR_CUDA;
     return QMM_OK;
@@ -343,6 +376,8 @@ qmm_status qmm_last_device_error(void *stream) {
     if (v && cudaMemcpy(di.status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return QMM_ERR_CUDA;
     return v == 0 ? QMM_OK : (qmm_status)v;
 }
+
+void qmm_set_static_weights(int on) { g_static_weights.store(on ? 1 : 0); }
 
 void qmm_set_wait_limit(uint64_t cycles) {
     if (cycles < 1) cycles = 1;

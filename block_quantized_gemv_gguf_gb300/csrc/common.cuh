@@ -55,11 +55,22 @@ __device__ __forceinline__ float byte_as_128_plus(uint32_t w) {
 
 // 32-bit little-endian load from shared memory at a 2-byte aligned address.
 __device__ __forceinline__ uint32_t lds_u32_a2(const uint8_t *p) {
-    uintptr_t a = reinterpret_cast<uintptr_t>(p);
-    if ((a & 3u) == 0) return *reinterpret_cast<const uint32_t *>(p);
-    const uint32_t *q = reinterpret_cast<const uint32_t *>(a & ~(uintptr_t)3);
+    // pointer arithmetic (not an integer round trip) keeps the state space
+    // of p visible to the compiler
+    const uint32_t mis = (uint32_t)reinterpret_cast<uintptr_t>(p) & 3u;
+    const uint32_t *q = reinterpret_cast<const uint32_t *>(p - mis);
+    if (mis == 0) return q[0];
     return __funnelshift_r(q[0], q[1], 16);
 }
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch.  Without the launch attribute both are
+// no-ops.  launch_dependents lets the next kernel on the stream be scheduled
+// once every CTA of this grid has issued it; wait blocks until the preceding
+// grid has completed and its memory is visible.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // ---------------------------------------------------------------------------
 // mbarrier
@@ -93,6 +104,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// As mbar_try_wait, but the thread may sleep up to `ns` nanoseconds (waking
+// as soon as the phase completes) before the call returns false.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
         : "memory");
     return ok != 0;
 }

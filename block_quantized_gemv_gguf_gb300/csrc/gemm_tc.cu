@@ -209,7 +209,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     constexpr int SA = L::SA;
     constexpr int RAWB = Raw<F>::bytes;
     extern __shared__ uint8_t smem_dyn[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~(uintptr_t)1023);
+    // 1024-byte aligned base derived from the shared array (keeps the
+    // accesses below in the shared window)
+    uint8_t *smem = smem_dyn + ((1024u - (smem_u32(smem_dyn) & 1023u)) & 1023u);
     uint8_t *sA = smem + L::OFF_A;
     uint8_t *sX = smem + L::OFF_X;
     uint8_t *sRaw = smem + L::OFF_RAW;
@@ -251,6 +253,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_d = *tmem_slot;
+    pdl_launch_dependents();
 
     if (warp == WARP_WPROD) {
         if (lane == 0) {
@@ -274,6 +277,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     } else if (warp == WARP_XPROD) {
         if (lane == 0) {
+            // Weights stream from the start; X (which may be written by the
+            // preceding kernel, e.g. the bf16 conversion) only after it ends.
+            pdl_wait();
             int issued = 0;
             for (int t = 0; t < nsteps; ++t) {
                 const int s = t % SA;
@@ -344,6 +350,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         // Epilogue: TMEM lane = tile row.  Warp w may only touch lanes 32*(w%4)..+31.
         const bool acc_ok = mbar_wait(acc_full, 0, 2 * drain_limit);
+        pdl_wait();   // Y: order after the preceding kernel
         tc_fence_after();
         if (__all_sync(0xffffffffu, acc_ok && !*abort_flag)) {
             const int q = warp & 3;
@@ -387,8 +394,18 @@ cudaError_t launch_one(const GemmArgs &a, const CUtensorMap &wmap, const CUtenso
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit);
     }
-    dim3 grid((unsigned)((a.M + BM - 1) / BM), (unsigned)((a.N + BN - 1) / BN));
-    kern<<<grid, NUM_THREADS, L::SMEM, st>>>(wmap, xmap, (int)a.M, (int)a.K, a.N, a.Y, a.status, a.wait_limit);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((a.M + BM - 1) / BM), (unsigned)((a.N + BN - 1) / BN), 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = L::SMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = a.pdl ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, kern, wmap, xmap, (int)a.M, (int)a.K, a.N, a.Y, a.status, a.wait_limit);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -86,21 +86,42 @@ template <int F, int NT, int CW> struct GL {
 // ---------------------------------------------------------------------------
 // small device helpers
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t bsub2(uint32_t a, uint32_t b) {
+// a + nb (bf16x2); nb holds the negated offsets, so the subtraction of the
+// magic-number offset is one plain add
+__device__ __forceinline__ uint32_t badd2(uint32_t a, uint32_t nb) {
     uint32_t r;
-    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(nb));
     return r;
 }
 // bf16x2 (M + b0, M + b1) from bytes 0,1 (SEL01) or 2,3 (SEL23) of `v`,
 // where M is the bf16 whose high byte is `hi` (0x43: 128, 0x45: 2048).
-template <uint32_t HI>
-__device__ __forceinline__ uint32_t pair01(uint32_t v) { return __byte_perm(v, HI, 0x4140u); }
-template <uint32_t HI>
-__device__ __forceinline__ uint32_t pair23(uint32_t v) { return __byte_perm(v, HI, 0x4342u); }
+// The constant in a register the compiler may not rematerialize (one
+// register for the whole loop instead of an immediate load per use).
+template <uint32_t C>
+__device__ __forceinline__ uint32_t in_reg() {
+    uint32_t r;
+    asm("mov.b32 %0, %1;" : "=r"(r) : "n"(C));
+    return r;
+}
+
+// hi: a register holding HI in its low byte.
+__device__ __forceinline__ uint32_t pair01(uint32_t v, uint32_t hi) { return __byte_perm(v, hi, 0x4140u); }
+__device__ __forceinline__ uint32_t pair23(uint32_t v, uint32_t hi) { return __byte_perm(v, hi, 0x4342u); }
 
 constexpr uint32_t BF2(uint32_t h) { return h | (h << 16); }   // bf16 pair from one bf16 bit pattern
-constexpr uint32_t C128 = BF2(0x4300u), C136 = BF2(0x4308u), C160 = BF2(0x4320u), C2176 = BF2(0x4508u);
+// negated offsets -128, -136, -160, -2176 as bf16 pairs
+constexpr uint32_t C128 = BF2(0xC300u), C136 = BF2(0xC308u), C160 = BF2(0xC320u), C2176 = BF2(0xC508u);
 
+// d = A * B (zero accumulator, no register initialization needed)
+__device__ __forceinline__ void mma16816_z(float (&d)[4], const uint32_t (&a)[4], uint2 b) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%10,%10,%10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b.x), "r"(b.y), "f"(0.f));
+}
+
+// d += A * B
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint2 b) {
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
@@ -109,13 +130,16 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b.x), "r"(b.y));
 }
 
-// A fragment from two words of byte codes (row g, row g+8): elements 4t..4t+3.
-template <uint32_t HI, uint32_t OFFS>
-__device__ __forceinline__ void afrag(uint32_t (&a)[4], uint32_t vg, uint32_t vg8) {
-    a[0] = bsub2(pair01<HI>(vg), OFFS);
-    a[1] = bsub2(pair01<HI>(vg8), OFFS);
-    a[2] = bsub2(pair23<HI>(vg), OFFS);
-    a[3] = bsub2(pair23<HI>(vg8), OFFS);
+
+// A fragment from two words of byte codes (row g, row g+8): elements 4t..4t+3;
+// offs = the negated offset pair (so the code value is pair + offs).
+template <uint32_t HI>
+__device__ __forceinline__ void afrag(uint32_t (&a)[4], uint32_t vg, uint32_t vg8, uint32_t offs) {
+    const uint32_t hi = in_reg<HI>();
+    a[0] = badd2(pair01(vg, hi), offs);
+    a[1] = badd2(pair01(vg8, hi), offs);
+    a[2] = badd2(pair23(vg, hi), offs);
+    a[3] = badd2(pair23(vg8, hi), offs);
 }
 
 __device__ __forceinline__ uint16_t lds_u16(const uint8_t *p) { return *reinterpret_cast<const uint16_t *>(p); }
@@ -158,7 +182,7 @@ __device__ __forceinline__ bool gwait(volatile unsigned *abort_flag, uint64_t *b
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     for (;;) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, 2000u)) return true;
         if (*abort_flag) return false;
         if ((uint64_t)(clock64() - t0) > limit) {
             *abort_flag = 1u;
@@ -279,11 +303,17 @@ __device__ __forceinline__ void acc_scaled(float *acc, const float (&d)[4], floa
     ffma2(acc[2], acc[3], sg8, sg8, d[2], d[3]);
 }
 
-// Entries e0..e0+7 (e0 a multiple of 8) of row r of the scale table.
-__device__ __forceinline__ void ld_scales8(float (&v)[8], const float *sct, int r, int e0) {
-    const float4 a = *reinterpret_cast<const float4 *>(sct + sct_index(r, e0));
-    const float4 b = *reinterpret_cast<const float4 *>(sct + sct_index(r, e0 + 4));
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+// Entries e0..e0+NE-1 (e0 a multiple of 4) of row r of the scale table.
+template <int NE>
+__device__ __forceinline__ void ld_scales(float (&v)[NE], const float *sct, int r, int e0) {
+#pragma unroll
+    for (int i = 0; i < NE; i += 4) {
+        const float4 a = *reinterpret_cast<const float4 *>(sct + sct_index(r, e0 + i));
+        v[i] = a.x;
+        v[i + 1] = a.y;
+        v[i + 2] = a.z;
+        v[i + 3] = a.w;
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -291,14 +321,21 @@ __device__ __forceinline__ void ld_scales8(float (&v)[8], const float *sct, int 
 // Row windows start 16-byte aligned (Q6_K: + woff, even); every 32-bit code
 // word is read with its alignment known at compile time (MIS: woff % 4 == 2).
 // ---------------------------------------------------------------------------
-template <int F, int NT, int P, bool MIS>
+template <int KSTR, int JSTR>
+__device__ __forceinline__ uint2 bfrag(const uint8_t *xb, int ks, int j) {
+    return *reinterpret_cast<const uint2 *>(xb + ks * KSTR + j * JSTR);
+}
+
+// xb: this lane's B fragment of k-step 0, tile 0 of the chunk; fragment
+// (ks, j) is at xb + ks * KSTR + j * JSTR.
+template <int F, int NT, int P, bool MIS, int KSTR, int JSTR>
 __device__ __forceinline__ void compute_chunk(float (&acc)[NT][4], const uint8_t *rg, const uint8_t *rg8,
-                                              const uint2 *xs, const float *sct, int r, const float *sx, int lane,
-                                              int t) {
+                                              const uint8_t *xb, const float *sct, int r, const float *sx, int t) {
+    const uint32_t k128 = in_reg<C128>(), k136 = in_reg<C136>(), k160 = in_reg<C160>(), k2176 = in_reg<C2176>();
     if constexpr (F == Q4_0) {
         float sg[8], sg8[8];
-        ld_scales8(sg, sct, r, 0);
-        ld_scales8(sg8, sct, r + 8, 0);
+        ld_scales<8>(sg, sct, r, 0);
+        ld_scales<8>(sg8, sct, r + 8, 0);
 #pragma unroll
         for (int bp = 0; bp < 4; ++bp) {            // blocks 2bp, 2bp+1: 36 bytes from a 4-aligned start
             const uint8_t *pg = rg + 36 * bp, *pg8 = rg8 + 36 * bp;
@@ -310,21 +347,21 @@ __device__ __forceinline__ void compute_chunk(float (&acc)[NT][4], const uint8_t
                 const int b = 2 * bp + bb;
                 const uint32_t wg = bb ? qog : qeg, wg8 = bb ? qog8 : qeg8;
                 uint32_t a0[4], a1[4];
-                afrag<0x43u, C136>(a0, wg & 0x0F0F0F0Fu, wg8 & 0x0F0F0F0Fu);
-                afrag<0x43u, C136>(a1, (wg >> 4) & 0x0F0F0F0Fu, (wg8 >> 4) & 0x0F0F0F0Fu);
+                afrag<0x43u>(a0, wg & 0x0F0F0F0Fu, wg8 & 0x0F0F0F0Fu, k136);
+                afrag<0x43u>(a1, (wg >> 4) & 0x0F0F0F0Fu, (wg8 >> 4) & 0x0F0F0F0Fu, k136);
 #pragma unroll
                 for (int j = 0; j < NT; ++j) {
-                    float d[4] = {0.f, 0.f, 0.f, 0.f};
-                    mma16816(d, a0, xs[((2 * b) * NT + j) * 32 + lane]);
-                    mma16816(d, a1, xs[((2 * b + 1) * NT + j) * 32 + lane]);
+                    float d[4];
+                    mma16816_z(d, a0, bfrag<KSTR, JSTR>(xb, 2 * b, j));
+                    mma16816(d, a1, bfrag<KSTR, JSTR>(xb, 2 * b + 1, j));
                     acc_scaled(acc[j], d, sg[b], sg8[b]);
                 }
             }
         }
     } else if constexpr (F == Q8_0) {
         float sg[8], sg8[8];
-        ld_scales8(sg, sct, r, 0);
-        ld_scales8(sg8, sct, r + 8, 0);
+        ld_scales<8>(sg, sct, r, 0);
+        ld_scales<8>(sg8, sct, r + 8, 0);
 #pragma unroll
         for (int b = 0; b < 8; ++b) {
             // block b at 34 b: odd blocks have 4-aligned codes, even blocks 2 mod 4
@@ -336,14 +373,14 @@ __device__ __forceinline__ void compute_chunk(float (&acc)[NT][4], const uint8_t
                 const uint32_t ug = ((b & 1) ? ld32(pg + o) : ld32_off2(pg + o)) ^ 0x80808080u;
                 const uint32_t ug8 = ((b & 1) ? ld32(pg8 + o) : ld32_off2(pg8 + o)) ^ 0x80808080u;
                 // q = 16 * (hi - 8) + lo with hi, lo the nibbles of q + 128
-                afrag<0x43u, C128>(al[grp], ug & 0x0F0F0F0Fu, ug8 & 0x0F0F0F0Fu);
-                afrag<0x45u, C2176>(ah[grp], (ug >> 4) & 0x0F0F0F0Fu, (ug8 >> 4) & 0x0F0F0F0Fu);
+                afrag<0x43u>(al[grp], ug & 0x0F0F0F0Fu, ug8 & 0x0F0F0F0Fu, k128);
+                afrag<0x45u>(ah[grp], (ug >> 4) & 0x0F0F0F0Fu, (ug8 >> 4) & 0x0F0F0F0Fu, k2176);
             }
 #pragma unroll
             for (int j = 0; j < NT; ++j) {
-                float d[4] = {0.f, 0.f, 0.f, 0.f};
-                const uint2 b0 = xs[((2 * b) * NT + j) * 32 + lane], b1 = xs[((2 * b + 1) * NT + j) * 32 + lane];
-                mma16816(d, al[0], b0);
+                float d[4];
+                const uint2 b0 = bfrag<KSTR, JSTR>(xb, 2 * b, j), b1 = bfrag<KSTR, JSTR>(xb, 2 * b + 1, j);
+                mma16816_z(d, al[0], b0);
                 mma16816(d, ah[0], b0);
                 mma16816(d, al[1], b1);
                 mma16816(d, ah[1], b1);
@@ -352,10 +389,10 @@ __device__ __forceinline__ void compute_chunk(float (&acc)[NT][4], const uint8_t
         }
     } else if constexpr (F == Q4_K) {
         float dsg[8], dsg8[8], dmg[8], dmg8[8];
-        ld_scales8(dsg, sct, r, 0);
-        ld_scales8(dsg8, sct, r + 8, 0);
-        ld_scales8(dmg, sct, r, 8);
-        ld_scales8(dmg8, sct, r + 8, 8);
+        ld_scales<8>(dsg, sct, r, 0);
+        ld_scales<8>(dsg8, sct, r + 8, 0);
+        ld_scales<8>(dmg, sct, r, 8);
+        ld_scales<8>(dmg8, sct, r + 8, 8);
         const uint8_t *qg = rg + 16, *qg8 = rg8 + 16;
 #pragma unroll
         for (int pr = 0; pr < 4; ++pr) {            // sub-blocks 2pr (low nibbles), 2pr+1 (high)
@@ -365,13 +402,13 @@ __device__ __forceinline__ void compute_chunk(float (&acc)[NT][4], const uint8_t
             for (int hn = 0; hn < 2; ++hn) {
                 const int s = 2 * pr + hn, sh = 4 * hn;
                 uint32_t a0[4], a1[4];
-                afrag<0x43u, C128>(a0, (w0g >> sh) & 0x0F0F0F0Fu, (w0g8 >> sh) & 0x0F0F0F0Fu);
-                afrag<0x43u, C128>(a1, (w1g >> sh) & 0x0F0F0F0Fu, (w1g8 >> sh) & 0x0F0F0F0Fu);
+                afrag<0x43u>(a0, (w0g >> sh) & 0x0F0F0F0Fu, (w0g8 >> sh) & 0x0F0F0F0Fu, k128);
+                afrag<0x43u>(a1, (w1g >> sh) & 0x0F0F0F0Fu, (w1g8 >> sh) & 0x0F0F0F0Fu, k128);
 #pragma unroll
                 for (int j = 0; j < NT; ++j) {
-                    float d[4] = {0.f, 0.f, 0.f, 0.f};
-                    mma16816(d, a0, xs[((2 * s) * NT + j) * 32 + lane]);
-                    mma16816(d, a1, xs[((2 * s + 1) * NT + j) * 32 + lane]);
+                    float d[4];
+                    mma16816_z(d, a0, bfrag<KSTR, JSTR>(xb, 2 * s, j));
+                    mma16816(d, a1, bfrag<KSTR, JSTR>(xb, 2 * s + 1, j));
                     // w = d*sc*q - dmin*m  =>  sum w x = (d sc) sum q x - (dmin m) sum x
                     acc_scaled(acc[j], d, dsg[s], dsg8[s]);
                     if constexpr (P == 2) {       // min term once per token (on the hi piece)
@@ -388,13 +425,8 @@ __device__ __forceinline__ void compute_chunk(float (&acc)[NT][4], const uint8_t
         }
     } else {  // Q6_K: element e = 128h + 32J + l, l = 16 lh + 4t + i, k-step G = 8h + 2J + lh
         float sg[16], sg8[16];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float4 a = *reinterpret_cast<const float4 *>(sct + sct_index(r, 4 * q));
-            const float4 b = *reinterpret_cast<const float4 *>(sct + sct_index(r + 8, 4 * q));
-            sg[4 * q] = a.x; sg[4 * q + 1] = a.y; sg[4 * q + 2] = a.z; sg[4 * q + 3] = a.w;
-            sg8[4 * q] = b.x; sg8[4 * q + 1] = b.y; sg8[4 * q + 2] = b.z; sg8[4 * q + 3] = b.w;
-        }
+        ld_scales<16>(sg, sct, r, 0);
+        ld_scales<16>(sg8, sct, r + 8, 0);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
 #pragma unroll
@@ -411,16 +443,99 @@ __device__ __forceinline__ void compute_chunk(float (&acc)[NT][4], const uint8_t
                     const uint32_t qg = ((lwg >> ns) & 0x0F0F0F0Fu) | (((hg >> (2 * J)) & 0x03030303u) << 4);
                     const uint32_t qg8 = ((lwg8 >> ns) & 0x0F0F0F0Fu) | (((hg8 >> (2 * J)) & 0x03030303u) << 4);
                     uint32_t a[4];
-                    afrag<0x43u, C160>(a, qg, qg8);
+                    afrag<0x43u>(a, qg, qg8, k160);
 #pragma unroll
                     for (int j = 0; j < NT; ++j) {
-                        float d[4] = {0.f, 0.f, 0.f, 0.f};
-                        mma16816(d, a, xs[(G * NT + j) * 32 + lane]);
+                        float d[4];
+                        mma16816_z(d, a, bfrag<KSTR, JSTR>(xb, G, j));
                         acc_scaled(acc[j], d, sg[G], sg8[G]);
                     }
                 }
             }
         }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// End of a tile: without a K split every compute thread stores its rows; with
+// one, partials go to shared memory [row][token] and cluster rank 0 sums the
+// KS slices in rank order (deterministic) and stores.
+// ---------------------------------------------------------------------------
+template <int NT, int P, int CW, int RG>
+__device__ __forceinline__ void finish_tile(const float (&acc)[RG][NT][4], float *sred, float *__restrict__ Y, int M,
+                                            int N, int m0, int KS, bool aborted, int warp, int lane) {
+    constexpr int ROWS = 16 * CW * RG;
+    if (KS == 1) {
+        if (warp < CW && !aborted) {
+            const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+            for (int q = 0; q < RG; ++q) {
+                const int r0 = m0 + 16 * (RG * warp + q) + g, r1 = r0 + 8;
+#pragma unroll
+                for (int j = 0; j < NT; ++j) {
+                    if constexpr (P == 2) {
+                        const int n = 4 * j + t;
+                        if (n < N) {
+                            if (r0 < M) Y[(int64_t)n * M + r0] = acc[q][j][0] + acc[q][j][1];
+                            if (r1 < M) Y[(int64_t)n * M + r1] = acc[q][j][2] + acc[q][j][3];
+                        }
+                    } else {
+                        const int n0 = 8 * j + 2 * t;
+                        if (n0 < N) {
+                            if (r0 < M) Y[(int64_t)n0 * M + r0] = acc[q][j][0];
+                            if (r1 < M) Y[(int64_t)n0 * M + r1] = acc[q][j][2];
+                        }
+                        if (n0 + 1 < N) {
+                            if (r0 < M) Y[(int64_t)(n0 + 1) * M + r0] = acc[q][j][1];
+                            if (r1 < M) Y[(int64_t)(n0 + 1) * M + r1] = acc[q][j][3];
+                        }
+                    }
+                }
+            }
+        }
+    } else {
+        // partials -> shared memory [row][token] (aliases the X fragments:
+        // wait until every warp of the CTA is done with them); rank 0 of the
+        // cluster sums
+        __syncthreads();
+        if (warp < CW) {
+            const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+            for (int q = 0; q < RG; ++q) {
+                const int r0 = 16 * (RG * warp + q) + g, r1 = r0 + 8;
+#pragma unroll
+                for (int j = 0; j < NT; ++j) {
+                    if constexpr (P == 2) {
+                        const int n = 4 * j + t;
+                        if (n < 16) {
+                            sred[r0 * 16 + n] = acc[q][j][0] + acc[q][j][1];
+                            sred[r1 * 16 + n] = acc[q][j][2] + acc[q][j][3];
+                        }
+                    } else {
+                        const int n0 = 8 * j + 2 * t;
+                        if (n0 + 1 < 16) {
+                            sred[r0 * 16 + n0] = acc[q][j][0];
+                            sred[r0 * 16 + n0 + 1] = acc[q][j][1];
+                            sred[r1 * 16 + n0] = acc[q][j][2];
+                            sred[r1 * 16 + n0 + 1] = acc[q][j][3];
+                        }
+                    }
+                }
+            }
+        }
+        cluster_sync_all();
+        if (cluster_ctarank() == 0 && warp < CW) {
+            // rank r's CTA holds K-slice r; every CTA of the cluster ran the
+            // same number of barriers, so an abort anywhere shows here only
+            // through the status word.
+            for (int idx = threadIdx.x; idx < ROWS * N; idx += CW * 32) {
+                const int row = idx / N, n = idx % N;
+                float v = 0.f;
+                for (int r = 0; r < KS; ++r) v += ld_dsmem_f32(sred + row * 16 + n, (uint32_t)r);
+                if (m0 + row < M && !aborted) Y[(int64_t)n * M + m0 + row] = v;
+            }
+        }
+        cluster_sync_all();
     }
 }
 
@@ -431,7 +546,9 @@ __global__ void __launch_bounds__(GL<F, NT, CW>::THREADS)
     using L = GL<F, NT, CW>;
     constexpr int S = L::S, XR = L::XR, ROWS = L::ROWS;
     extern __shared__ uint8_t smem_dyn[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~(uintptr_t)1023);
+    // 1024-byte aligned base, derived from the shared array itself so that
+    // every access below compiles to a shared-window load or store
+    uint8_t *smem = smem_dyn + ((1024u - (smem_u32(smem_dyn) & 1023u)) & 1023u);
     uint8_t *sstage = smem + L::OFF_STAGE;
     uint8_t *sxraw = smem + L::OFF_XRAW;
     uint8_t *sxr = smem + L::OFF_XR;
@@ -471,10 +588,11 @@ __global__ void __launch_bounds__(GL<F, NT, CW>::THREADS)
         fence_barrier_init();
     }
     __syncthreads();
+    pdl_launch_dependents();
 
-    float acc[NT][4];
+    float acc[1][NT][4];
 #pragma unroll
-    for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+    for (int j = 0; j < NT; ++j) acc[0][j][0] = acc[0][j][1] = acc[0][j][2] = acc[0][j][3] = 0.f;
 
     if (warp == L::WARP_TMA) {
         // ---------------- TMA producers: lane 0 weights, lane 1 raw X ----------------
@@ -497,6 +615,7 @@ __global__ void __launch_bounds__(GL<F, NT, CW>::THREADS)
                     (void)mbar_wait(&full[c % S], (c / S) & 1, drain_limit);
         } else if (lane == 1) {
             prefetch_tensormap(&xmap);
+            pdl_wait();   // X may come from the preceding kernel
             constexpr int XRS = L::XRS;
             int issued = 0;
             for (int c = 0; c < nloc; ++c) {
@@ -513,6 +632,7 @@ __global__ void __launch_bounds__(GL<F, NT, CW>::THREADS)
         }
     } else {
         // ---------------- compute warps ----------------
+        pdl_wait();   // Y is written below: order after the preceding kernel
         const int g = lane >> 2, t = lane & 3;
         const int rg = 16 * warp + g;         // tile rows of this thread: rg, rg + 8
         // Build this warp's share of the X fragments of local chunk c.
@@ -549,12 +669,12 @@ __global__ void __launch_bounds__(GL<F, NT, CW>::THREADS)
                 break;
             const uint8_t *pg = raw + rg * L::WIN + woff;
             const uint8_t *slot = sxr + xs * L::XSLOT;
-            const uint2 *xsl = reinterpret_cast<const uint2 *>(slot);
+            const uint8_t *xb = slot + 8 * lane;
             const float *sxl = reinterpret_cast<const float *>(slot + L::XS);
             if (F == Q6_K && (woff & 2))
-                compute_chunk<F, NT, P, true>(acc, pg, pg + 8 * L::WIN, xsl, sct, rg, sxl, lane, t);
+                compute_chunk<F, NT, P, true, NT * 256, 256>(acc[0], pg, pg + 8 * L::WIN, xb, sct, rg, sxl, t);
             else
-                compute_chunk<F, NT, P, false>(acc, pg, pg + 8 * L::WIN, xsl, sct, rg, sxl, lane, t);
+                compute_chunk<F, NT, P, false, NT * 256, 256>(acc[0], pg, pg + 8 * L::WIN, xb, sct, rg, sxl, t);
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&empty[s]);
@@ -563,140 +683,377 @@ __global__ void __launch_bounds__(GL<F, NT, CW>::THREADS)
         }
     }
 
-    // ---------------- reduction over the K split and store ----------------
     const bool aborted = *abort_flag != 0u;
-    if (KS == 1) {
-        if (warp < CW && !aborted) {
-            const int g = lane >> 2, t = lane & 3;
-            const int r0 = m0 + 16 * warp + g, r1 = r0 + 8;
-#pragma unroll
-            for (int j = 0; j < NT; ++j) {
-                if constexpr (P == 2) {
-                    const int n = 4 * j + t;
-                    if (n < N) {
-                        if (r0 < M) Y[(int64_t)n * M + r0] = acc[j][0] + acc[j][1];
-                        if (r1 < M) Y[(int64_t)n * M + r1] = acc[j][2] + acc[j][3];
-                    }
-                } else {
-                    const int n0 = 8 * j + 2 * t;
-                    if (n0 < N) {
-                        if (r0 < M) Y[(int64_t)n0 * M + r0] = acc[j][0];
-                        if (r1 < M) Y[(int64_t)n0 * M + r1] = acc[j][2];
-                    }
-                    if (n0 + 1 < N) {
-                        if (r0 < M) Y[(int64_t)(n0 + 1) * M + r0] = acc[j][1];
-                        if (r1 < M) Y[(int64_t)(n0 + 1) * M + r1] = acc[j][3];
-                    }
-                }
-            }
-        }
-    } else {
-        // partials -> shared memory [row][token] (aliases the X ring: wait until
-        // every warp of the CTA is done with it); rank 0 of the cluster sums
-        __syncthreads();
-        if (warp < CW) {
-            const int g = lane >> 2, t = lane & 3;
-            const int r0 = 16 * warp + g, r1 = r0 + 8;
-#pragma unroll
-            for (int j = 0; j < NT; ++j) {
-                if constexpr (P == 2) {
-                    const int n = 4 * j + t;
-                    if (n < 16) {
-                        sred[r0 * 16 + n] = acc[j][0] + acc[j][1];
-                        sred[r1 * 16 + n] = acc[j][2] + acc[j][3];
-                    }
-                } else {
-                    const int n0 = 8 * j + 2 * t;
-                    if (n0 + 1 < 16) {
-                        sred[r0 * 16 + n0] = acc[j][0];
-                        sred[r0 * 16 + n0 + 1] = acc[j][1];
-                        sred[r1 * 16 + n0] = acc[j][2];
-                        sred[r1 * 16 + n0 + 1] = acc[j][3];
-                    }
-                }
-            }
-        }
-        cluster_sync_all();
-        if (cluster_ctarank() == 0 && warp < CW) {
-            // rank r's CTA holds K-slice r; every CTA of the cluster ran the
-            // same number of barriers, so an abort anywhere shows here only
-            // through the status word.
-            for (int idx = threadIdx.x; idx < ROWS * N; idx += CW * 32) {
-                const int row = idx / N, n = idx % N;
-                float v = 0.f;
-                for (int r = 0; r < KS; ++r) v += ld_dsmem_f32(sred + row * 16 + n, (uint32_t)r);
-                if (m0 + row < M && !aborted) Y[(int64_t)n * M + m0 + row] = v;
-            }
-        }
-        cluster_sync_all();
-    }
+    finish_tile<NT, P, CW, 1>(acc, sred, Y, M, N, m0, KS, aborted, warp, lane);
     if (threadIdx.x == 0 && aborted) report_status(status, kStatusTimeout);
 }
 
-template <int F, int NT, int P, bool XBF16, int CW>
-cudaError_t launch_t(const CUtensorMap &wmap, const CUtensorMap &xmap, int64_t M, int64_t K, int N, float *Y,
-                     int num_sms, unsigned *status, uint64_t limit, cudaStream_t st) {
-    using L = GL<F, NT, CW>;
-    constexpr int ROWS = L::ROWS;
-    auto kern = gemv_mma_kernel<F, NT, P, XBF16, CW>;
-    static std::atomic<uint64_t> configured{0};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (!(configured.load() & (1ull << (dev & 63)))) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
-        if (e != cudaSuccess) return e;
-        configured.fetch_or(1ull << (dev & 63));
+// ---------------------------------------------------------------------------
+// Resident-X variant for a single MMA column tile (P * N <= 8 columns: the
+// decode GEMV and a few tokens).  The B fragments of the CTA's whole K slice
+// are built once, straight from global X, while the first weight stages are
+// in flight; after that the compute warps only wait for weights.  Lanes of
+// MMA columns past the used ones read a zero area with the same stride, so
+// every fragment load is a plain shared load with a compile-time offset.
+// ---------------------------------------------------------------------------
+template <int F, int NC, int CW, int RG> struct GR {
+    static constexpr int ROWS = 16 * CW * RG;                // RG groups of 16 rows per compute warp
+    static constexpr int WARP_TMA = CW;
+    static constexpr int THREADS = (CW + 1) * 32;
+    static constexpr int WIN = GWin<F>::bytes;
+    static constexpr int STAGE = ROWS * WIN;                 // multiple of 1024
+    static constexpr int S = CW * RG >= 8 ? 2 : 3;           // weight stages
+    static constexpr int XRES = 16384;                       // resident B fragments
+    static constexpr int KSB = NC * 32;                      // fragment bytes per k-step
+    static constexpr int MAXC = XRES / (16 * KSB);           // chunks a CTA may own
+    static constexpr int ZB = NC < 8 ? 16 * KSB : 0;         // zero fragments (unused columns)
+    static constexpr int SXB = F == Q4_K ? MAXC * 8 * 16 * 4 : 0;   // Q4_K sub-block sums of x
+    static constexpr int SCT = ROWS * SCW * 4;
+    static constexpr int OFF_STAGE = 0;
+    static constexpr int OFF_X = S * STAGE;
+    static constexpr int OFF_Z = OFF_X + XRES;
+    static constexpr int OFF_SX = OFF_Z + ZB;
+    static constexpr int OFF_SCT = OFF_SX + SXB;
+    // The raw X slice [N][K slice] lands in the fragment area itself: it has
+    // the same size (P * N columns of 2-byte pieces = N rows of 4/P-byte
+    // elements) and is converted in place (all reads, barrier, all writes).
+    static constexpr int OFF_XRAW = OFF_X;
+    static constexpr int OFF_RED = OFF_X;                    // reused after the last chunk
+    static constexpr int OFF_BAR = OFF_SCT + SCT;
+    static constexpr int OFF_MISC = OFF_BAR + (2 * S + 1) * 8;
+    static constexpr int SMEM = OFF_MISC + 16 + 1024;
+    static_assert(ROWS * 16 * 4 <= XRES, "reduction buffer fits in the fragment area");
+    static_assert(STAGE % 1024 == 0 && OFF_BAR % 8 == 0, "alignment");
+    static_assert(SMEM <= 232448, "shared memory");
+};
+
+template <int F, int NC, int P, bool XBF16, int CW, int RG>
+__global__ void __launch_bounds__(GR<F, NC, CW, RG>::THREADS)
+    gemv_res_kernel(const __grid_constant__ CUtensorMap wmap, const void *__restrict__ Xv, int M, int K, int N,
+                    float *__restrict__ Y, int cps, unsigned *status, uint64_t wait_limit) {
+    using L = GR<F, NC, CW, RG>;
+    constexpr int S = L::S;
+    extern __shared__ uint8_t smem_dyn[];
+    uint8_t *smem = smem_dyn + ((1024u - (smem_u32(smem_dyn) & 1023u)) & 1023u);
+    uint8_t *sstage = smem + L::OFF_STAGE;
+    uint8_t *sfrag = smem + L::OFF_X;
+    uint8_t *szero = smem + L::OFF_Z;
+    float *ssx = reinterpret_cast<float *>(smem + L::OFF_SX);
+    float *sct = reinterpret_cast<float *>(smem + L::OFF_SCT);
+    float *sred = reinterpret_cast<float *>(smem + L::OFF_RED);
+    const uint8_t *sxraw = smem + L::OFF_XRAW;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::OFF_BAR);
+    uint64_t *empty = full + S;
+    uint64_t *xfull = empty + S;
+    volatile unsigned *abort_flag = reinterpret_cast<volatile unsigned *>(smem + L::OFF_MISC);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.x * L::ROWS;
+    const int nchunks = K / KC;
+    const int c_begin = blockIdx.y * cps;
+    const int c_end = min(nchunks, c_begin + cps);
+    const int nloc = c_end > c_begin ? c_end - c_begin : 0;
+    const int KS = gridDim.y;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], CW);
+        }
+        mbar_init(xfull, 1);
+        *abort_flag = 0u;
+        fence_barrier_init();
     }
-    const int tiles = (int)((M + ROWS - 1) / ROWS);
-    const int nchunks = (int)(K / KC);
+    __syncthreads();
+    pdl_launch_dependents();
+    constexpr int XES = XBF16 ? 2 : 4;
+    const int kslice = nloc * KC;   // elements of the K slice
+
+    float acc[RG][1][4];
+#pragma unroll
+    for (int q = 0; q < RG; ++q) acc[q][0][0] = acc[q][0][1] = acc[q][0][2] = acc[q][0][3] = 0.f;
+    if (warp == L::WARP_TMA) {
+        if (lane == 0) {
+            const uint64_t drain_limit = wait_limit < (1ull << 31) ? (1ull << 31) : wait_limit;
+            prefetch_tensormap(&wmap);
+            int issued = 0;
+            bool x_issued = false;
+            for (int c = 0; c < nloc; ++c) {
+                const int s = c % S;
+                if (c >= S && !gwait(abort_flag, &empty[s], ((c / S) - 1) & 1, wait_limit)) break;
+                if (*abort_flag) break;
+                const int cg = c_begin + c;
+                const int xb = F == Q6_K ? ((210 * cg) & ~15) : cg * L::WIN;
+                mbar_arrive_expect_tx(&full[s], (uint32_t)L::STAGE);
+                tma_load_2d(sstage + s * L::STAGE, &wmap, &full[s], xb >> 1, m0);
+                issued = c + 1;
+                if (c == (nloc < S ? nloc : S) - 1) {
+                    // Weights are read before the preceding kernel on the
+                    // stream has finished (they must not be written by it);
+                    // X only after it.
+                    pdl_wait();
+                    // the X slice, one contiguous row piece per token (16-byte
+                    // aligned: K and the slice start are multiples of 256)
+                    const uint32_t rowb = (uint32_t)kslice * XES;
+                    mbar_arrive_expect_tx(xfull, rowb * (uint32_t)N);
+                    for (int n = 0; n < N; ++n)
+                        tma_load_1d(smem + L::OFF_XRAW + n * rowb,
+                                    static_cast<const uint8_t *>(Xv) + ((int64_t)n * K + (int64_t)c_begin * KC) * XES,
+                                    rowb, xfull);
+                    x_issued = true;
+                }
+            }
+            if (*abort_flag) {
+                for (int c = issued - S < 0 ? 0 : issued - S; c < issued; ++c)
+                    (void)mbar_wait(&full[c % S], (c / S) & 1, drain_limit);
+                if (x_issued) (void)mbar_wait(xfull, 0, drain_limit);
+            }
+        }
+    } else {
+        // ---- B fragments of the slice, converted in place from the staged X:
+        // item it = (ks * NC + col) * 4 + t; every thread first reads all of
+        // its items into registers, then (after a barrier) writes them ----
+        pdl_wait();   // Y is written below: order after the preceding kernel
+        const int tid = threadIdx.x;
+        const bool x_ok = nloc == 0 || __all_sync(0xffffffffu, gwait(abort_flag, xfull, 0, wait_limit));
+        constexpr int IPT = (L::MAXC * 16 * NC * 4 + CW * 32 - 1) / (CW * 32);   // items per thread, at most
+        const int nitems = nloc * 16 * NC * 4;
+        uint2 fr[IPT];
+#pragma unroll
+        for (int i = 0; i < IPT; ++i) {
+            const int it = tid + i * CW * 32;
+            fr[i] = make_uint2(0u, 0u);
+            if (x_ok && it < nitems) {
+                const int t = it & 3, col = (it >> 2) % NC, ks = (it >> 2) / NC;
+                const int n = col / P, p = col % P;
+                if (n < N) {
+                    const int e = n * kslice + 16 * ks + 4 * t;
+                    if constexpr (XBF16) {
+                        fr[i] = *reinterpret_cast<const uint2 *>(sxraw + 2 * e);
+                    } else {
+                        const float4 f = *reinterpret_cast<const float4 *>(sxraw + 4 * e);
+                        const uint32_t hi01 = pack_bf16x2(f.x, f.y), hi23 = pack_bf16x2(f.z, f.w);
+                        if (P == 1 || p == 0) {
+                            fr[i] = make_uint2(hi01, hi23);
+                        } else {
+                            fr[i].x = pack_bf16x2(f.x - __uint_as_float(hi01 << 16),
+                                                  f.y - __uint_as_float(hi01 & 0xFFFF0000u));
+                            fr[i].y = pack_bf16x2(f.z - __uint_as_float(hi23 << 16),
+                                                  f.w - __uint_as_float(hi23 & 0xFFFF0000u));
+                        }
+                    }
+                }
+            }
+        }
+        if constexpr (F == Q4_K) {
+            // ssx[c][s][n] = sum of x[n] over sub-block s of local chunk c (separate area)
+            for (int it = tid; it < nloc * 128; it += CW * 32) {
+                const int n = it & 15, sb = (it >> 4) & 7, c = it >> 7;
+                float a = 0.f;
+                if (x_ok && n < N) {
+                    const int e = n * kslice + c * KC + 32 * sb;
+                    if constexpr (XBF16) {
+                        const uint4 *x = reinterpret_cast<const uint4 *>(sxraw + 2 * e);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const uint4 u = x[q];
+                            a += (__uint_as_float(u.x << 16) + __uint_as_float(u.x & 0xFFFF0000u)) +
+                                 (__uint_as_float(u.y << 16) + __uint_as_float(u.y & 0xFFFF0000u));
+                            a += (__uint_as_float(u.z << 16) + __uint_as_float(u.z & 0xFFFF0000u)) +
+                                 (__uint_as_float(u.w << 16) + __uint_as_float(u.w & 0xFFFF0000u));
+                        }
+                    } else {
+                        const float4 *x = reinterpret_cast<const float4 *>(sxraw + 4 * e);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            const float4 v = x[q];
+                            a += (v.x + v.y) + (v.z + v.w);
+                        }
+                    }
+                }
+                ssx[it] = a;
+            }
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(CW * 32) : "memory");   // every raw read is done
+#pragma unroll
+        for (int i = 0; i < IPT; ++i) {
+            const int it = tid + i * CW * 32;
+            if (it < nitems) *reinterpret_cast<uint2 *>(sfrag + 8 * it) = fr[i];
+        }
+        for (int it = tid; it < L::ZB / 8; it += CW * 32) *reinterpret_cast<uint2 *>(szero + 8 * it) = make_uint2(0u, 0u);
+        asm volatile("bar.sync 1, %0;" ::"r"(CW * 32) : "memory");   // compute warps only
+
+        const int g = lane >> 2, t = lane & 3;
+        const uint8_t *xb0 = g < NC ? sfrag + 8 * (4 * g + t) : szero + 8 * t;
+        const int cstride = g < NC ? 16 * L::KSB : 0;
+        for (int c = 0; c < nloc && x_ok; ++c) {
+            const int s = c % S;
+            const int cg = c_begin + c;
+            const int woff = F == Q6_K ? ((210 * cg) & 15) : 0;
+            if (!__all_sync(0xffffffffu, gwait(abort_flag, &full[s], (c / S) & 1, wait_limit) && !*abort_flag))
+                break;
+            const uint8_t *raw = sstage + s * L::STAGE;
+#pragma unroll
+            for (int q = 0; q < RG; ++q) prep_scales<F>(sct, raw, woff, RG * warp + q, lane);
+            __syncwarp();
+            const uint8_t *xb = xb0 + c * cstride;
+            const float *sxl = ssx + c * 128;
+            // the RG row groups are independent MMA chains (and share the
+            // B fragments), which the scheduler interleaves
+#pragma unroll
+            for (int q = 0; q < RG; ++q) {
+                const int rg = 16 * (RG * warp + q) + g;
+                const uint8_t *pg = raw + rg * L::WIN + woff;
+                if (F == Q6_K && (woff & 2))
+                    compute_chunk<F, 1, P, true, L::KSB, 0>(acc[q], pg, pg + 8 * L::WIN, xb, sct, rg, sxl, t);
+                else
+                    compute_chunk<F, 1, P, false, L::KSB, 0>(acc[q], pg, pg + 8 * L::WIN, xb, sct, rg, sxl, t);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+        }
+    }
+
+    const bool aborted = *abort_flag != 0u;
+    finish_tile<1, P, CW, RG>(acc, sred, Y, M, N, m0, KS, aborted, warp, lane);
+    if (threadIdx.x == 0 && aborted) report_status(status, kStatusTimeout);
+}
+
+// K split: the smallest power of two (<= 8, one cluster) that gives at
+// least 1.5 CTAs per SM, and (max_cps > 0) few enough chunks per CTA for the
+// resident fragments.  Returns 0 if the slice cannot be made small enough.
+int plan_ks(int64_t tiles, int nchunks, int num_sms, int max_cps, int force) {
     int ks = 1;
-    while (ks < 8 && (int64_t)tiles * ks * 2 < (int64_t)num_sms * 3 && ks * 2 <= nchunks) ks *= 2;
+    if (force > 0) {
+        while (ks < force && ks < 8 && ks * 2 <= nchunks) ks *= 2;
+    } else {
+        while (ks < 8 && tiles * ks * 2 < (int64_t)num_sms * 3 && ks * 2 <= nchunks) ks *= 2;
+    }
+    while (max_cps > 0 && (nchunks + ks - 1) / ks > max_cps && ks < 8 && ks * 2 <= nchunks) ks *= 2;
+    if (max_cps > 0 && (nchunks + ks - 1) / ks > max_cps) return 0;
+    return ks;
+}
+
+// x_arg: the kernel's second parameter (X tensor map or X address).
+template <typename Kern, typename XArg>
+cudaError_t launch_cluster(Kern kern, int smem, int threads, int64_t tiles, int ks, int nchunks, cudaStream_t st,
+                           bool pdl, const CUtensorMap &wmap, const XArg &x_arg, int64_t M, int64_t K, int N,
+                           float *Y, unsigned *status, uint64_t limit) {
     const int cps = (nchunks + ks - 1) / ks;
     ks = (nchunks + cps - 1) / cps;   // no empty slices
-    // cluster dims must divide the grid: round ks up to a power of two
-    int ksp = 1;
+    int ksp = 1;                      // cluster dims must divide the grid
     while (ksp < ks) ksp *= 2;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)tiles, (unsigned)ksp, 1);
-    cfg.blockDim = dim3(L::THREADS, 1, 1);
-    cfg.dynamicSmemBytes = L::SMEM;
+    cfg.blockDim = dim3((unsigned)threads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 1;
-    attr[0].val.clusterDim.y = (unsigned)ksp;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    unsigned na = 0;
+    if (ksp > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = 1;
+        attr[na].val.clusterDim.y = (unsigned)ksp;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = ksp > 1 ? 1 : 0;
-    e = cudaLaunchKernelEx(&cfg, kern, wmap, xmap, (int)M, (int)K, N, Y, cps, status, limit);
+    cfg.numAttrs = na;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, wmap, x_arg, (int)M, (int)K, N, Y, cps, status, limit);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
+template <typename Kern>
+cudaError_t set_smem_once(Kern kern, int smem, std::atomic<uint64_t> &configured) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (!(configured.load() & (1ull << (dev & 63)))) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        configured.fetch_or(1ull << (dev & 63));
+    }
+    return cudaSuccess;
+}
+
+struct GemvCall {
+    const CUtensorMap *wmap, *xmap;
+    const void *X;
+    int64_t M, K;
+    int N;
+    float *Y;
+    GemvPlan plan;
+    bool pdl;
+    unsigned *status;
+    uint64_t limit;
+    cudaStream_t st;
+};
+
+template <int F, int NT, int P, bool XBF16, int CW>
+cudaError_t launch_ring(const GemvCall &c) {
+    using L = GL<F, NT, CW>;
+    if (c.plan.rows != L::ROWS) return cudaErrorInvalidValue;   // must match the weight map's box
+    auto kern = gemv_mma_kernel<F, NT, P, XBF16, CW>;
+    static std::atomic<uint64_t> configured{0};
+    cudaError_t e = set_smem_once(kern, L::SMEM, configured);
+    if (e != cudaSuccess) return e;
+    const int64_t tiles = (c.M + L::ROWS - 1) / L::ROWS;
+    return launch_cluster(kern, L::SMEM, L::THREADS, tiles, c.plan.ks, (int)(c.K / KC), c.st, c.pdl, *c.wmap,
+                          *c.xmap, c.M, c.K, c.N, c.Y, c.status, c.limit);
+}
+
+template <int F, int NC, int P, bool XBF16, int CW, int RG>
+cudaError_t launch_res(const GemvCall &c) {
+    using L = GR<F, NC, CW, RG>;
+    if (c.plan.rows != L::ROWS) return cudaErrorInvalidValue;   // must match the weight map's box
+    const int nchunks = (int)(c.K / KC);
+    if ((nchunks + c.plan.ks - 1) / c.plan.ks > L::MAXC) return cudaErrorInvalidValue;
+    auto kern = gemv_res_kernel<F, NC, P, XBF16, CW, RG>;
+    static std::atomic<uint64_t> configured{0};
+    cudaError_t e = set_smem_once(kern, L::SMEM, configured);
+    if (e != cudaSuccess) return e;
+    const int64_t tiles = (c.M + L::ROWS - 1) / L::ROWS;
+    return launch_cluster(kern, L::SMEM, L::THREADS, tiles, c.plan.ks, nchunks, c.st, c.pdl, *c.wmap, c.X, c.M,
+                          c.K, c.N, c.Y, c.status, c.limit);
+}
+
+template <int F, int NC, int P, bool XBF16>
+cudaError_t launch_res_tile(const GemvCall &c) {
+    if (c.plan.rows == 64) return launch_res<F, NC, P, XBF16, 4, 1>(c);
+    if (c.plan.rows == 128)
+        return c.plan.rg == 2 ? launch_res<F, NC, P, XBF16, 4, 2>(c) : launch_res<F, NC, P, XBF16, 8, 1>(c);
+    return launch_res<F, NC, P, XBF16, 8, 2>(c);
+}
+
 template <int F, int NT, int P, bool XBF16>
-cudaError_t launch_cw(const CUtensorMap &wmap, const CUtensorMap &xmap, int64_t M, int64_t K, int N, float *Y,
-                      int num_sms, unsigned *status, uint64_t limit, cudaStream_t st) {
-    if (gemv_tile_rows(M, num_sms) == 128)
-        return launch_t<F, NT, P, XBF16, 8>(wmap, xmap, M, K, N, Y, num_sms, status, limit, st);
-    return launch_t<F, NT, P, XBF16, 4>(wmap, xmap, M, K, N, Y, num_sms, status, limit, st);
+cudaError_t launch_cw(const GemvCall &c) {
+    if (c.plan.resident) {
+        if (NT != 1) return cudaErrorInvalidValue;
+        return P * c.N == 1 ? launch_res_tile<F, 1, P, XBF16>(c) : launch_res_tile<F, 2, P, XBF16>(c);
+    }
+    if (c.plan.rows == 128) return launch_ring<F, NT, P, XBF16, 8>(c);
+    return launch_ring<F, NT, P, XBF16, 4>(c);
 }
 
 template <int F, bool XBF16>
-cudaError_t launch_f(const CUtensorMap &wmap, const CUtensorMap &xmap, int64_t M, int64_t K, int N, float *Y,
-                     int num_sms, unsigned *status, uint64_t limit, cudaStream_t st) {
+cudaError_t launch_f(const GemvCall &c) {
     constexpr int P = XBF16 ? 1 : 2;
-    const int cols = P * N;
-    const int nt = (cols + 7) / 8;
+    const int nt = (P * c.N + 7) / 8;
     if constexpr (XBF16) {
-        if (nt <= 1) return launch_cw<F, 1, 1, true>(wmap, xmap, M, K, N, Y, num_sms, status, limit, st);
-        return launch_cw<F, 2, 1, true>(wmap, xmap, M, K, N, Y, num_sms, status, limit, st);
+        if (nt <= 1) return launch_cw<F, 1, 1, true>(c);
+        return launch_cw<F, 2, 1, true>(c);
     } else {
         switch (nt) {
-        case 1: return launch_cw<F, 1, 2, false>(wmap, xmap, M, K, N, Y, num_sms, status, limit, st);
-        case 2: return launch_cw<F, 2, 2, false>(wmap, xmap, M, K, N, Y, num_sms, status, limit, st);
-        case 3: return launch_cw<F, 3, 2, false>(wmap, xmap, M, K, N, Y, num_sms, status, limit, st);
-        default: return launch_cw<F, 4, 2, false>(wmap, xmap, M, K, N, Y, num_sms, status, limit, st);
+        case 1: return launch_cw<F, 1, 2, false>(c);
+        case 2: return launch_cw<F, 2, 2, false>(c);
+        case 3: return launch_cw<F, 3, 2, false>(c);
+        default: return launch_cw<F, 4, 2, false>(c);
         }
     }
 }
@@ -719,19 +1076,42 @@ int gemv_window_bytes(int fmt) {
     }
 }
 
-cudaError_t launch_gemv_mma(int fmt, const CUtensorMap &wmap, const CUtensorMap &xmap, int xbf16, int64_t M,
-                            int64_t K, int N, float *Y, int num_sms, unsigned *status, uint64_t limit,
-                            cudaStream_t st) {
-    if (N < 1 || N > 16) return cudaErrorInvalidValue;
+GemvPlan plan_gemv(int64_t M, int64_t K, int N, int xbf16, int num_sms, const GemvTuning &tun) {
+    GemvPlan p{};
+    const int cols = (xbf16 ? 1 : 2) * N;
+    const int nchunks = (int)(K / KC);
+    int rows = tun.rows ? tun.rows : gemv_tile_rows(M, num_sms);
+    if (tun.resident && cols <= 2) {
+        // MAXC of the resident layout: 16 KB of fragments, cols * 32 bytes per k-step
+        const int maxc = 16384 / (16 * 32 * cols);
+        const int rg = rows == 256 ? 2 : (rows == 128 ? (tun.rg == 2 ? 2 : 1) : 1);
+        const int64_t tiles = (M + rows - 1) / rows;
+        const int ks = plan_ks(tiles, nchunks, num_sms, maxc, tun.ks);
+        if (ks > 0) {
+            p.resident = 1;
+            p.rows = rows;
+            p.rg = rg;
+            p.ks = ks;
+            return p;
+        }
+    }
+    p.resident = 0;
+    p.rows = rows >= 128 ? 128 : 64;
+    p.rg = 1;
+    p.ks = plan_ks((M + p.rows - 1) / p.rows, nchunks, num_sms, 0, tun.ks);
+    return p;
+}
+
+cudaError_t launch_gemv_mma(int fmt, const GemvPlan &plan, const CUtensorMap &wmap, const CUtensorMap &xmap,
+                            const void *X, int xbf16, int64_t M, int64_t K, int N, float *Y, bool pdl,
+                            unsigned *status, uint64_t limit, cudaStream_t st) {
+    if (N < 1 || N > 16 || plan.ks < 1 || plan.ks > 8) return cudaErrorInvalidValue;
+    const GemvCall c{&wmap, &xmap, X, M, K, N, Y, plan, pdl, status, limit, st};
     switch (fmt) {
-    case Q8_0: return xbf16 ? launch_f<Q8_0, true>(wmap, xmap, M, K, N, Y, num_sms, status, limit, st)
-                            : launch_f<Q8_0, false>(wmap, xmap, M, K, N, Y, num_sms, status, limit, st);
-    case Q4_0: return xbf16 ? launch_f<Q4_0, true>(wmap, xmap, M, K, N, Y, num_sms, status, limit, st)
-                            : launch_f<Q4_0, false>(wmap, xmap, M, K, N, Y, num_sms, status, limit, st);
-    case Q4_K: return xbf16 ? launch_f<Q4_K, true>(wmap, xmap, M, K, N, Y, num_sms, status, limit, st)
-                            : launch_f<Q4_K, false>(wmap, xmap, M, K, N, Y, num_sms, status, limit, st);
-    case Q6_K: return xbf16 ? launch_f<Q6_K, true>(wmap, xmap, M, K, N, Y, num_sms, status, limit, st)
-                            : launch_f<Q6_K, false>(wmap, xmap, M, K, N, Y, num_sms, status, limit, st);
+    case Q8_0: return xbf16 ? launch_f<Q8_0, true>(c) : launch_f<Q8_0, false>(c);
+    case Q4_0: return xbf16 ? launch_f<Q4_0, true>(c) : launch_f<Q4_0, false>(c);
+    case Q4_K: return xbf16 ? launch_f<Q4_K, true>(c) : launch_f<Q4_K, false>(c);
+    case Q6_K: return xbf16 ? launch_f<Q6_K, true>(c) : launch_f<Q6_K, false>(c);
     default: return cudaErrorInvalidValue;
     }
 }

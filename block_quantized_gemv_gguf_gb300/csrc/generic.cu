@@ -67,16 +67,26 @@ __global__ void __launch_bounds__(256) gemv_generic_kernel(const uint8_t *__rest
     }
 }
 
+// 8 elements per thread per step (two 16-byte loads, one 16-byte store) when
+// X and out are 16-byte aligned; grid-stride, so any count is covered.
 __global__ void x_to_bf16_kernel(const float *__restrict__ X, int64_t count, __nv_bfloat16 *__restrict__ out) {
-    const int64_t i4 = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) * 4;
-    if (i4 + 3 < count && (reinterpret_cast<uintptr_t>(X) & 15) == 0) {
-        const float4 v = *reinterpret_cast<const float4 *>(X + i4);
-        out[i4] = __float2bfloat16_rn(v.x);
-        out[i4 + 1] = __float2bfloat16_rn(v.y);
-        out[i4 + 2] = __float2bfloat16_rn(v.z);
-        out[i4 + 3] = __float2bfloat16_rn(v.w);
-    } else {
-        for (int64_t i = i4; i < count && i < i4 + 4; ++i) out[i] = __float2bfloat16_rn(X[i]);
+    pdl_launch_dependents();
+    pdl_wait();   // X may come from the preceding kernel
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x * 8;
+    const bool vec = ((reinterpret_cast<uintptr_t>(X) | reinterpret_cast<uintptr_t>(out)) & 15) == 0;
+    for (int64_t i8 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8; i8 < count; i8 += stride) {
+        if (vec && i8 + 7 < count) {
+            const float4 a = *reinterpret_cast<const float4 *>(X + i8);
+            const float4 b = *reinterpret_cast<const float4 *>(X + i8 + 4);
+            uint4 o;
+            o.x = pack_bf16x2(a.x, a.y);
+            o.y = pack_bf16x2(a.z, a.w);
+            o.z = pack_bf16x2(b.x, b.y);
+            o.w = pack_bf16x2(b.z, b.w);
+            *reinterpret_cast<uint4 *>(out + i8) = o;
+        } else {
+            for (int64_t i = i8; i < count && i < i8 + 8; ++i) out[i] = __float2bfloat16_rn(X[i]);
+        }
     }
 }
 
@@ -120,10 +130,19 @@ cudaError_t launch_gemv_generic(int fmt, const uint8_t *W, int64_t M, int64_t K,
     return cudaGetLastError();
 }
 
-cudaError_t launch_x_to_bf16(const float *X, int64_t count, uint16_t *out, cudaStream_t st) {
+cudaError_t launch_x_to_bf16(const float *X, int64_t count, uint16_t *out, bool pdl, cudaStream_t st) {
     if (count <= 0) return cudaSuccess;
-    const int g = grid_for((count + 3) / 4, 256);
-    x_to_bf16_kernel<<<g, 256, 0, st>>>(X, count, reinterpret_cast<__nv_bfloat16 *>(out));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid_for((count + 7) / 8, 256), 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, x_to_bf16_kernel, X, count, reinterpret_cast<__nv_bfloat16 *>(out));
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -14,12 +14,33 @@ cudaError_t launch_dequant(int fmt, const uint8_t *W, int64_t M, int64_t K, floa
 cudaError_t launch_gemv_generic(int fmt, const uint8_t *W, int64_t M, int64_t K, const void *X, int xbf16,
                                 int N, float *Y, cudaStream_t st);
 
+// Requested launch shape of the tensor-core GEMV (0 = automatic).
+struct GemvTuning {
+    int rows;       // rows per tile: 64, 128 or 256
+    int rg;         // 16-row groups per compute warp of the resident-X kernel (1 or 2)
+    int ks;         // K split (cluster size, 1..8)
+    int resident;   // 0 disables the resident-X kernel
+};
+
+// What will run: the resident-X kernel (P * N <= 2 MMA columns) or the ring
+// kernel, its tile height (= the weight tensor map's box height), row groups
+// per warp and K split.
+struct GemvPlan {
+    int resident;
+    int rows;
+    int rg;
+    int ks;
+};
+GemvPlan plan_gemv(int64_t M, int64_t K, int N, int xbf16, int num_sms, const GemvTuning &tun);
+
 // Tensor-core GEMV, 1 <= N <= 16 (K % 256 == 0, 16-byte aligned W rows and
-// X).  wmap: raw weight bytes as u16 [M][row_bytes/2], box {window/2, 64};
-// xmap: X [N][K] (f32 or bf16), box {256, N}.
-cudaError_t launch_gemv_mma(int fmt, const CUtensorMap &wmap, const CUtensorMap &xmap, int xbf16, int64_t M,
-                            int64_t K, int N, float *Y, int num_sms, unsigned *status, uint64_t limit,
-                            cudaStream_t st);
+// X), executing `plan`.  wmap: raw weight bytes as u16 [M][row_bytes/2], box
+// {window/2, plan.rows}; xmap: X [N][K] (f32 or bf16), box {256, N}; X: the
+// same tensor by address.  pdl: launched as a programmatic dependent of the
+// preceding kernel (weights are read before it ends).
+cudaError_t launch_gemv_mma(int fmt, const GemvPlan &plan, const CUtensorMap &wmap, const CUtensorMap &xmap,
+                            const void *X, int xbf16, int64_t M, int64_t K, int N, float *Y, bool pdl,
+                            unsigned *status, uint64_t limit, cudaStream_t st);
 
 // Raw bytes of one 256-weight chunk of a row in the GEMV's staging.
 int gemv_window_bytes(int fmt);
@@ -27,8 +48,9 @@ int gemv_window_bytes(int fmt);
 // Rows per GEMV tile (the weight tensor map's box height) for M rows.
 int gemv_tile_rows(int64_t M, int num_sms);
 
-// bf16 out[i] = round-to-nearest-even(X[i]).
-cudaError_t launch_x_to_bf16(const float *X, int64_t count, uint16_t *out, cudaStream_t st);
+// bf16 out[i] = round-to-nearest-even(X[i]).  pdl: launched as a
+// programmatic dependent of the preceding kernel.
+cudaError_t launch_x_to_bf16(const float *X, int64_t count, uint16_t *out, bool pdl, cudaStream_t st);
 
 // Tensor-core GEMM.  wmap: raw weight bytes viewed as u16 [M][row_bytes/2],
 // box {window/2, 128}; xmap: bf16 X [N][K], box {64, BN}, 128-byte swizzle.
@@ -40,6 +62,7 @@ struct GemmArgs {
     float *Y;
     unsigned *status;
     uint64_t wait_limit;
+    int pdl;         // programmatic dependent launch (weights read before the preceding kernel ends)
 };
 cudaError_t launch_gemm_tc(const GemmArgs &a, const CUtensorMap &wmap, const CUtensorMap &xmap, cudaStream_t st);
 

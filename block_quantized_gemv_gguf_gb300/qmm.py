@@ -27,7 +27,7 @@ GEMV_MAX_N, GEMM_MAX_N = 16, 512
 BLOCK = {Q8_0: (32, 34), Q4_0: (32, 18), Q4_K: (256, 144), Q6_K: (256, 210)}
 EXPORTS = ("qmm_gemv", "qmm_gemm", "qmm_gemm_workspace_bytes", "qmm_matmul", "qmm_matmul_host",
            "qmm_dequant", "qmm_block_info", "qmm_last_device_error", "qmm_status_str",
-           "qmm_set_wait_limit")
+           "qmm_set_wait_limit", "qmm_set_static_weights")
 
 _lock = threading.Lock()
 _lib = None
@@ -66,6 +66,8 @@ def load() -> ctypes.CDLL:
         lib.qmm_status_str.restype = ctypes.c_char_p
         lib.qmm_set_wait_limit.argtypes = [ctypes.c_uint64]
         lib.qmm_set_wait_limit.restype = None
+        lib.qmm_set_static_weights.argtypes = [ctypes.c_int]
+        lib.qmm_set_static_weights.restype = None
         for f in ("qmm_gemv", "qmm_gemm", "qmm_matmul", "qmm_matmul_host", "qmm_dequant", "qmm_block_info",
                   "qmm_last_device_error"):
             getattr(lib, f).restype = ci
@@ -167,6 +169,12 @@ def qmm_set_wait_limit(cycles: int) -> None:
 # --------------------------------------------------------------------------
 # convenience wrappers (allocate the output, raise on error)
 # --------------------------------------------------------------------------
+def qmm_set_static_weights(on: bool) -> None:
+    """Static-weights mode (see include/qmm.h): weights stream before the
+    preceding kernel on the stream ends; W must not be written meanwhile."""
+    load().qmm_set_static_weights(1 if on else 0)
+
+
 def _check(s: int, what: str):
     if s != OK:
         raise QmmError(s, what)

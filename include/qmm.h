@@ -201,6 +201,21 @@ QMM_API qmm_status qmm_last_device_error(void *stream);
 QMM_API const char *qmm_status_str(qmm_status s);
 
 /*
+ * Static-weights mode, process wide, for launches issued after the call
+ * (default off; the environment variable QMM_STATIC_WEIGHTS=1 turns it on
+ * until this function is first called).  On: the tensor-core GEMV and GEMM
+ * and the GEMM's bf16 conversion are launched as programmatic dependents of
+ * the preceding kernel on the stream, and each starts streaming its weight
+ * blocks W before that kernel has finished; X is read and Y written only
+ * after it has.  This hides most of the launch and first-byte latency of a
+ * chain of projections (a decode step).  The caller promises that no kernel
+ * on the stream writes W between the calls that read it (weights loaded once
+ * and then only read, as in inference); otherwise leave it off.  The pages
+ * have no counterpart: it is a property of how calls are queued on a GPU.
+ */
+QMM_API void qmm_set_static_weights(int on);
+
+/*
  * Test hook: upper bound, in SM clock cycles, on every device-side wait of
  * the tensor-core GEMM (default about two seconds).  A tiny limit makes the
  * waits give up, which tests use to exercise the QMM_ERR_TIMEOUT path

@@ -1,0 +1,68 @@
+"""GPU parity of every GEMV launch shape, forced through the library's tuning
+overrides (rows per tile, K split, resident-X on or off).
+
+The overrides are read once per process, so each combination runs in a child
+process that checks a few shapes against the oracle and prints one line.
+"""
+from __future__ import annotations
+
+import os
+import subprocess
+import sys
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+CHILD = r'''
+import numpy as np, torch, oracle
+from block_quantized_gemv_gguf_gb300 import qmm, synth
+qmm.load()
+bad = []
+for wt in (synth.Q8_0, synth.Q4_0, synth.Q4_K, synth.Q6_K):
+    for (M, K) in ((300, 4096), (77, 2048)):
+        w = synth.gen_weights(wt, M, K, "tune")
+        W = torch.from_numpy(w).cuda()
+        for N in (1, 2, 3, 5, 8, 16):
+            for bf in (False, True):
+                x = synth.gen_x(N, K, "tune")
+                xo = synth.f32_to_bf16_bits(x) if bf else x
+                X = torch.from_numpy(xo).cuda()
+                if bf:
+                    X = X.view(torch.bfloat16)
+                Y = torch.full((N, M), float("nan"), device="cuda")
+                s = qmm.qmm_gemv(wt, W, M, K, X, N, Y)
+                torch.cuda.synchronize()
+                if s != qmm.OK:
+                    bad.append((wt, M, K, N, bf, qmm.status_name(s)))
+                    continue
+                Yr, S = oracle.matmul(wt, w, M, K, xo)
+                ok, ratio = oracle.within(Y.cpu().numpy(), Yr, S, 1e-5, 1e-6)
+                if not ok:
+                    bad.append((wt, M, K, N, bf, ratio))
+assert qmm.qmm_last_device_error() == qmm.OK
+print("BAD" if bad else "OK", bad)
+'''
+
+COMBOS = [
+    {"QMM_GEMV_ROWS": "64", "QMM_GEMV_KS": "1", "QMM_GEMV_RESIDENT": "1"},
+    {"QMM_GEMV_ROWS": "64", "QMM_GEMV_KS": "8", "QMM_GEMV_RESIDENT": "1"},
+    {"QMM_GEMV_ROWS": "128", "QMM_GEMV_RG": "2", "QMM_GEMV_KS": "2", "QMM_GEMV_RESIDENT": "1"},
+    {"QMM_GEMV_ROWS": "128", "QMM_GEMV_RG": "1", "QMM_GEMV_KS": "4", "QMM_GEMV_RESIDENT": "1"},
+    {"QMM_GEMV_ROWS": "256", "QMM_GEMV_KS": "1", "QMM_GEMV_RESIDENT": "1"},
+    {"QMM_GEMV_ROWS": "128", "QMM_GEMV_KS": "1", "QMM_GEMV_RESIDENT": "0"},
+    {"QMM_GEMV_ROWS": "64", "QMM_GEMV_KS": "4", "QMM_GEMV_RESIDENT": "0"},
+]
+
+
+@pytest.mark.parametrize("env", COMBOS, ids=lambda e: "-".join(f"{k[9:].lower()}{v}" for k, v in e.items()))
+def test_forced_launch_shapes(env):
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    r = subprocess.run([sys.executable, "-c", CHILD], cwd=ROOT, env={**os.environ, **env, "PYTHONPATH": ROOT},
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-3000:]
+    assert r.stdout.strip().startswith("OK"), r.stdout[-3000:]
