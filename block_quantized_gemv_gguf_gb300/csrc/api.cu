@@ -106,6 +106,7 @@ struct Settings {
     int gemv_max_n;   // QMM_GEMV_MAX_N: largest N qmm_matmul sends to the GEMV
     int force;        // QMM_FORCE_PATH: 0 none, 1 gemv, 2 gemm
     int gemm_bn;      // QMM_GEMM_BN: 0 = model-based choice
+    int gemm_cl;      // QMM_GEMM_CL: CTAs per cluster sharing X tiles (1, 2, 4); 0 = default
     int gemv_rows;    // QMM_GEMV_ROWS: 64, 128 or 256 rows per GEMV tile; 0 = by M
     int gemv_rg;      // QMM_GEMV_RG: 16-row groups per warp (1 or 2) of the resident-X GEMV
     int gemv_ks;      // QMM_GEMV_KS: K split of the GEMV (1..8); 0 = automatic
@@ -121,6 +122,8 @@ const Settings &settings() {
         t.force = (f && !std::strcmp(f, "gemv")) ? 1 : (f && !std::strcmp(f, "gemm")) ? 2 : 0;
         t.gemm_bn = env_int("QMM_GEMM_BN", 0);
         if (t.gemm_bn != 64 && t.gemm_bn != 128 && t.gemm_bn != 256) t.gemm_bn = 0;
+        t.gemm_cl = env_int("QMM_GEMM_CL", 0);
+        if (t.gemm_cl != 1 && t.gemm_cl != 2 && t.gemm_cl != 4) t.gemm_cl = 0;
         t.gemv_rows = env_int("QMM_GEMV_ROWS", 0);
         if (t.gemv_rows != 64 && t.gemv_rows != 128 && t.gemv_rows != 256) t.gemv_rows = 0;
         t.gemv_rg = env_int("QMM_GEMV_RG", 0) == 2 ? 2 : 1;
@@ -156,19 +159,19 @@ qmm_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QMM_OK : QMM_ERR
 int choose_bn(int64_t M, int64_t N, int num_sms) {
     const int forced = settings().gemm_bn;
     if (forced) return forced;
-    // Per 64-k stage a tile costs about max(dequant, MMA) cycles: the 128-row
-    // dequantization ~230 cycles, the MMA 2*BN cycles.  Pick the BN with the
-    // smallest (waves x stage time).
+    // A tile's 64-k stage costs about max(~1100 cycles of fixed pipeline
+    // latency, 4 * BN cycles of MMA and X traffic); pick the BN with the
+    // fewest (waves x stage cost), the larger grid on a tie.
     const int64_t tiles_m = (M + 127) / 128;
     int best = 64;
     double best_cost = 1e30;
-    for (int bn : {64, 128, 256}) {
+    for (int bn : {256, 128, 64}) {
         if (bn > 64 && N <= bn / 2) continue;   // a smaller tile covers N
         const int64_t tiles = tiles_m * ((N + bn - 1) / bn);
         const int64_t waves = (tiles + num_sms - 1) / num_sms;
-        const double stage = bn * 2.0 > 230.0 ? bn * 2.0 : 230.0;
-        const double cost = (double)waves * stage * (bn == 256 ? 0.98 : 1.0);
-        if (cost < best_cost) {
+        const double stage = bn * 4.0 > 1100.0 ? bn * 4.0 : 1100.0;
+        const double cost = (double)waves * stage;
+        if (cost <= best_cost) {
             best_cost = cost;
             best = bn;
         }
@@ -267,11 +270,12 @@ qmm_status gemm_impl(int wt, const void *W, size_t w_bytes, int64_t M, int64_t K
             return QMM_ERR_CUDA;
     }
     {
-        cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)N};
-        cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-        cuuint32_t box[2] = {64u, (cuuint32_t)bn};
-        cuuint32_t estr[2] = {1u, 1u};
-        if (enc(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(xb), dims, strides, box, estr,
+        // {64 k within a block, token, 64-k block}: one copy = XG stages
+        cuuint64_t dims[3] = {64u, (cuuint64_t)N, (cuuint64_t)(K / 64)};
+        cuuint64_t strides[2] = {(cuuint64_t)K * 2, 128u};
+        cuuint32_t box[3] = {64u, (cuuint32_t)bn, (cuuint32_t)gemm_x_stages_per_copy(bn)};
+        cuuint32_t estr[3] = {1u, 1u, 1u};
+        if (enc(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(xb), dims, strides, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return QMM_ERR_CUDA;
@@ -282,6 +286,7 @@ qmm_status gemm_impl(int wt, const void *W, size_t w_bytes, int64_t M, int64_t K
     a.K = K;
     a.N = (int)N;
     a.bn = bn;
+    a.cl = settings().gemm_cl ? settings().gemm_cl : 1;
     a.Y = Y;
     a.status = di.status;
     a.wait_limit = g_wait_limit.load();

@@ -161,14 +161,6 @@ __device__ __forceinline__ void ffma2(float &a0, float &a1, float s0, float s1, 
         : "f"(s0), "f"(s1), "f"(d0), "f"(d1));
 }
 
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
 __device__ __forceinline__ float ld_dsmem_f32(const float *local, uint32_t rank) {
     uint32_t la = smem_u32(local), ra;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(la), "r"(rank));

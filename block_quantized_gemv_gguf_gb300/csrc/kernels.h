@@ -53,18 +53,23 @@ int gemv_tile_rows(int64_t M, int num_sms);
 cudaError_t launch_x_to_bf16(const float *X, int64_t count, uint16_t *out, bool pdl, cudaStream_t st);
 
 // Tensor-core GEMM.  wmap: raw weight bytes viewed as u16 [M][row_bytes/2],
-// box {window/2, 128}; xmap: bf16 X [N][K], box {64, BN}, 128-byte swizzle.
+// box {window/2, 128}; xmap: bf16 X as a 3-D tensor {64 k, N tokens, K/64
+// k-blocks} (strides K*2 and 128 bytes), box {64, BN, XG}, 128-byte swizzle,
+// XG = gemm_x_stages_per_copy(BN).
 struct GemmArgs {
     int fmt;
     int64_t M, K;
     int N;
     int bn;          // token tile (64, 128 or 256)
+    int cl;          // CTAs per cluster sharing each X tile by multicast (1, 2 or 4)
     float *Y;
     unsigned *status;
     uint64_t wait_limit;
     int pdl;         // programmatic dependent launch (weights read before the preceding kernel ends)
 };
 cudaError_t launch_gemm_tc(const GemmArgs &a, const CUtensorMap &wmap, const CUtensorMap &xmap, cudaStream_t st);
+
+int gemm_x_stages_per_copy(int bn);
 
 // Window of raw weight bytes one 256-weight chunk of a row occupies in the
 // GEMM's shared-memory staging (bytes; a multiple of 16).

@@ -66,3 +66,49 @@ def test_forced_launch_shapes(env):
                        capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stderr[-3000:]
     assert r.stdout.strip().startswith("OK"), r.stdout[-3000:]
+
+
+GEMM_CHILD = r'''
+import numpy as np, torch, oracle
+from block_quantized_gemv_gguf_gb300 import qmm, synth
+qmm.load()
+bad = []
+for wt in (synth.Q4_0, synth.Q4_K, synth.Q6_K, synth.Q8_0):
+    for (M, K, N) in ((300, 2048, 100), (128, 2048, 17), (520, 4096, 512)):
+        w = synth.gen_weights(wt, M, K, "tune-gemm")
+        W = torch.from_numpy(w).cuda()
+        x = synth.gen_x(N, K, "tune-gemm")
+        X = torch.from_numpy(x).cuda()
+        Y = torch.full((N, M), float("nan"), device="cuda")
+        s = qmm.qmm_gemm(wt, W, M, K, X, N, Y, qmm.workspace_for(N, K, X))
+        torch.cuda.synchronize()
+        if s != qmm.OK:
+            bad.append((wt, M, K, N, qmm.status_name(s)))
+            continue
+        Yr, S = oracle.matmul(wt, w, M, K, x)
+        ok, ratio = oracle.within(Y.cpu().numpy(), Yr, S, 2e-3, 1e-5)
+        if not ok:
+            bad.append((wt, M, K, N, ratio))
+assert qmm.qmm_last_device_error() == qmm.OK
+print("BAD" if bad else "OK", bad)
+'''
+
+GEMM_COMBOS = [
+    {"QMM_GEMM_CL": "1", "QMM_GEMM_BN": "256"},
+    {"QMM_GEMM_CL": "2", "QMM_GEMM_BN": "64"},
+    {"QMM_GEMM_CL": "4", "QMM_GEMM_BN": "128"},
+    {"QMM_GEMM_CL": "4", "QMM_GEMM_BN": "256"},
+]
+
+
+@pytest.mark.parametrize("env", GEMM_COMBOS, ids=lambda e: "-".join(f"{k[9:].lower()}{v}" for k, v in e.items()))
+def test_forced_gemm_shapes(env):
+    """The tensor-core GEMM with every cluster size and token tile (M not a
+    multiple of the cluster's rows: the padding CTAs must stay silent)."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    r = subprocess.run([sys.executable, "-c", GEMM_CHILD], cwd=ROOT, env={**os.environ, **env, "PYTHONPATH": ROOT},
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-3000:]
+    assert r.stdout.strip().startswith("OK"), r.stdout[-3000:]
