@@ -144,6 +144,23 @@ class Clocks:
 
 
 # ---------------------------------------------------------------------------
+# multi-rank aggregation (each rank runs the whole step on its own GPU: weak
+# scaling, no data-path collective)
+# ---------------------------------------------------------------------------
+def max_over_ranks(values: dict, world: int, device) -> dict:
+    """Per-op times (ms per step), maximum over all ranks; unchanged when
+    world == 1.  Every rank must call it with the same keys."""
+    if world <= 1:
+        return dict(values)
+    import torch
+    import torch.distributed as dist
+    keys = sorted(values)
+    t = torch.tensor([float(values[k]) for k in keys], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return {k: float(v) for k, v in zip(keys, t.tolist())}
+
+
+# ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
 def run_gpu(args):
@@ -279,18 +296,15 @@ def run_gpu(args):
     for name, evs in events.items():
         med[name] = sum(a.elapsed_time(b) for (a, b), _ in evs) / K_steps
     steps_timed = K_steps
+    med = max_over_ranks(med, world, dev)      # the slowest rank sets the aggregate
     ms_step = sum(med.values())
-    if world > 1:
-        t = torch.tensor([ms_step], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(t.item())
 
     dec_bytes = sum(alg_bytes(synth.Q4_0, M, K, 1, 4) for M, K in DECODE_SHAPES)
     head_bytes = alg_bytes(synth.Q6_K, Mh, Kh, Nh, 4)
     pre_flops = sum(2.0 * M * K * PREFILL_N for M, K in PREFILL_SHAPES)
     decode_gbs = dec_bytes / (med["decode"] * 1e-3) / 1e9 * world if "decode" in med else None
-    head_gbs = head_bytes / (med["lmhead"] * 1e-3) / 1e9 if "lmhead" in med else None
-    pre_tflops = pre_flops / (med["prefill"] * 1e-3) / 1e12 if "prefill" in med else None
+    head_gbs = head_bytes / (med["lmhead"] * 1e-3) / 1e9 * world if "lmhead" in med else None
+    pre_tflops = pre_flops / (med["prefill"] * 1e-3) / 1e12 * world if "prefill" in med else None
 
     # dominant kernel of the step -> roofline object
     shares = {k: v / sum(med.values()) for k, v in med.items()}
