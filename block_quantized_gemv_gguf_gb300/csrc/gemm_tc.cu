@@ -66,7 +66,7 @@ template <int F, int BN> struct Layout {
     static constexpr int BUDGET = 227 * 1024 - 2048;
     static constexpr int SR = BUDGET - 2 * XSLOT >= 4 * RAW_BYTES ? 4 : (BUDGET - 2 * XSLOT >= 3 * RAW_BYTES ? 3 : 2);
     static constexpr int SX_FIT = (BUDGET - SR * RAW_BYTES) / XSLOT;
-    static constexpr int SX = SX_FIT > 8 ? 8 : SX_FIT;     // X copies in flight
+    static constexpr int SX = SX_FIT >= 8 ? 8 : (SX_FIT >= 4 ? 4 : SX_FIT);   // X copies in flight
     static_assert(SX >= 2, "at least two X slots");
     static constexpr int OFF_X = 0;
     static constexpr int OFF_RAW = OFF_X + SX * XSLOT;
@@ -303,15 +303,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     drain(&raw_full[c % SR], (c / SR) & 1, drain_limit);
         }
     } else if (warp == WARP_XPROD) {
-        if (lane == 0) {
+        // XL lanes may issue X copies side by side (lane l takes the rounds
+        // u = l, l + XL, ...); XL must divide SX, so that every slot belongs to
+        // exactly one lane and that lane's waits on it are in its own program
+        // order (a parity wait can then never alias a phase two ahead).
+        constexpr int XL = 1;   // several lanes were measured slower here; kept general for the lane split
+        static_assert(SX % XL == 0, "each X slot owned by one issuing lane");
+        if (lane < XL) {
             // Weights stream from the start; X (which may be written by the
             // preceding kernel, e.g. the bf16 conversion) only after it ends.
             pdl_wait();
-            int issued = 0;   // X copies (rounds of XG stages)
+            int issued = 0;   // X copies (rounds of XG stages) this lane issued: rounds lane + XL*i, i < issued
             const uint32_t leader_cempty = CL > 1 ? cluster_addr(x_cempty, 0u) : 0u;
             constexpr int XG = L::XG;
             const int nrounds = nsteps / XG;
-            for (int u = 0; u < nrounds; ++u) {
+            for (int u = lane; u < nrounds; u += XL) {
                 const int s = u % SX;
                 if (u >= SX && !wait_ok(ctl, &x_empty[s], ((u / SX) - 1) & 1, wait_limit)) break;
                 if (*abort_flag) break;
@@ -320,20 +326,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const int kb = kchunk(t0 / (KC / BK)) * (KC / BK) + t0 % (KC / BK);   // its 64-k block
                 if constexpr (CL == 1) {
                     tma_load_3d(sX + s * L::XSLOT, &xmap, &x_full[s], 0, n0, kb);
-                    issued = u + 1;
+                    ++issued;
                 } else {
                     mbar_arrive_remote(leader_cempty + 8u * (uint32_t)s);
                     if (crank == 0) {
                         if (!wait_ok(ctl, &x_cempty[s], (u / SX) & 1, wait_limit)) break;
                         tma_load_3d_mc(sX + s * L::XSLOT, &xmap, &x_full[s], 0, n0, kb, (uint16_t)((1u << CL) - 1u));
-                        issued = u + 1;
+                        ++issued;
                     }
                 }
             }
-            if (crank == 0) *x_issued = (unsigned)issued;
-            if (CL == 1 && *abort_flag)
-                for (int u = issued - SX < 0 ? 0 : issued - SX; u < issued; ++u)
-                    drain(&x_full[u % SX], (u / SX) & 1, drain_limit);
+            if (CL > 1 && crank == 0) *x_issued = (unsigned)issued;
+            if (CL == 1 && *abort_flag)   // drain this lane's copies that may still be in flight
+                for (int i = 0; i < issued; ++i) {
+                    const int u = lane + XL * i;
+                    if (u + SX >= lane + XL * issued) drain(&x_full[u % SX], (u / SX) & 1, drain_limit);
+                }
         }
     } else if (warp == WARP_MMA) {
         if (lane == 0) {

@@ -112,13 +112,26 @@ constexpr uint32_t BF2(uint32_t h) { return h | (h << 16); }   // bf16 pair from
 // negated offsets -128, -136, -160, -2176 as bf16 pairs
 constexpr uint32_t C128 = BF2(0xC300u), C136 = BF2(0xC308u), C160 = BF2(0xC320u), C2176 = BF2(0xC508u);
 
-// d = A * B (zero accumulator, no register initialization needed)
-__device__ __forceinline__ void mma16816_z(float (&d)[4], const uint32_t (&a)[4], uint2 b) {
+// A quad of zeros the compiler keeps in registers (the zero accumulator of
+// every first MMA of a block reads it; nothing re-zeroes registers per MMA).
+struct ZeroQuad {
+    float z[4];
+};
+__device__ __forceinline__ ZeroQuad zero_quad() {
+    ZeroQuad q;
+    asm("mov.b32 %0, 0;\n\tmov.b32 %1, 0;\n\tmov.b32 %2, 0;\n\tmov.b32 %3, 0;"
+        : "=f"(q.z[0]), "=f"(q.z[1]), "=f"(q.z[2]), "=f"(q.z[3]));
+    return q;
+}
+
+// d = A * B + 0
+__device__ __forceinline__ void mma16816_z(float (&d)[4], const uint32_t (&a)[4], uint2 b, const ZeroQuad &z) {
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%10,%10,%10,%10};"
+        "{%10,%11,%12,%13};"
         : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b.x), "r"(b.y), "f"(0.f));
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b.x), "r"(b.y), "f"(z.z[0]), "f"(z.z[1]), "f"(z.z[2]),
+          "f"(z.z[3]));
 }
 
 // d += A * B
@@ -324,6 +337,7 @@ template <int F, int NT, int P, bool MIS, int KSTR, int JSTR>
 __device__ __forceinline__ void compute_chunk(float (&acc)[NT][4], const uint8_t *rg, const uint8_t *rg8,
                                               const uint8_t *xb, const float *sct, int r, const float *sx, int t) {
     const uint32_t k128 = in_reg<C128>(), k136 = in_reg<C136>(), k160 = in_reg<C160>(), k2176 = in_reg<C2176>();
+    const ZeroQuad zq = zero_quad();
     if constexpr (F == Q4_0) {
         float sg[8], sg8[8];
         ld_scales<8>(sg, sct, r, 0);
@@ -344,7 +358,7 @@ __device__ __forceinline__ void compute_chunk(float (&acc)[NT][4], const uint8_t
 #pragma unroll
                 for (int j = 0; j < NT; ++j) {
                     float d[4];
-                    mma16816_z(d, a0, bfrag<KSTR, JSTR>(xb, 2 * b, j));
+                    mma16816_z(d, a0, bfrag<KSTR, JSTR>(xb, 2 * b, j), zq);
                     mma16816(d, a1, bfrag<KSTR, JSTR>(xb, 2 * b + 1, j));
                     acc_scaled(acc[j], d, sg[b], sg8[b]);
                 }
@@ -372,7 +386,7 @@ __device__ __forceinline__ void compute_chunk(float (&acc)[NT][4], const uint8_t
             for (int j = 0; j < NT; ++j) {
                 float d[4];
                 const uint2 b0 = bfrag<KSTR, JSTR>(xb, 2 * b, j), b1 = bfrag<KSTR, JSTR>(xb, 2 * b + 1, j);
-                mma16816_z(d, al[0], b0);
+                mma16816_z(d, al[0], b0, zq);
                 mma16816(d, ah[0], b0);
                 mma16816(d, al[1], b1);
                 mma16816(d, ah[1], b1);
@@ -399,7 +413,7 @@ __device__ __forceinline__ void compute_chunk(float (&acc)[NT][4], const uint8_t
 #pragma unroll
                 for (int j = 0; j < NT; ++j) {
                     float d[4];
-                    mma16816_z(d, a0, bfrag<KSTR, JSTR>(xb, 2 * s, j));
+                    mma16816_z(d, a0, bfrag<KSTR, JSTR>(xb, 2 * s, j), zq);
                     mma16816(d, a1, bfrag<KSTR, JSTR>(xb, 2 * s + 1, j));
                     // w = d*sc*q - dmin*m  =>  sum w x = (d sc) sum q x - (dmin m) sum x
                     acc_scaled(acc[j], d, dsg[s], dsg8[s]);
@@ -439,7 +453,7 @@ __device__ __forceinline__ void compute_chunk(float (&acc)[NT][4], const uint8_t
 #pragma unroll
                     for (int j = 0; j < NT; ++j) {
                         float d[4];
-                        mma16816_z(d, a, bfrag<KSTR, JSTR>(xb, G, j));
+                        mma16816_z(d, a, bfrag<KSTR, JSTR>(xb, G, j), zq);
                         acc_scaled(acc[j], d, sg[G], sg8[G]);
                     }
                 }
