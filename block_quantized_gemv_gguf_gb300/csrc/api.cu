@@ -136,8 +136,10 @@ const Settings &settings() {
 }
 
 // Common validation of W, M, K, X, N, Y.
+// ybytes_override: the size of the output actually written at Y (argmax
+// mode writes N entries, not N x M); 0 means N * M * 4.
 qmm_status validate(int wt, const void *W, size_t w_bytes, int64_t M, int64_t K, const void *X, int xt,
-                    int64_t N, const float *Y, int64_t max_n, int &E, int &B) {
+                    int64_t N, const float *Y, int64_t max_n, int &E, int &B, size_t ybytes_override = 0) {
     if (!block_geom(wt, E, B)) return QMM_ERR_INVALID_ARG;
     if (xt != QMM_X_F32 && xt != QMM_X_BF16) return QMM_ERR_INVALID_ARG;
     if (!W || !X || !Y) return QMM_ERR_INVALID_ARG;
@@ -148,7 +150,7 @@ qmm_status validate(int wt, const void *W, size_t w_bytes, int64_t M, int64_t K,
     if (w_bytes < need) return QMM_ERR_INVALID_ARG;
     const size_t xs = xt == QMM_X_F32 ? 4 : 2;
     if (((uintptr_t)X) % xs || ((uintptr_t)Y) % 4) return QMM_ERR_INVALID_ARG;
-    const size_t ybytes = (size_t)N * (size_t)M * 4;
+    const size_t ybytes = ybytes_override ? ybytes_override : (size_t)N * (size_t)M * 4;
     if (overlaps(Y, ybytes, W, need) || overlaps(Y, ybytes, X, (size_t)N * (size_t)K * xs))
         return QMM_ERR_INVALID_ARG;
     return QMM_OK;
@@ -179,10 +181,13 @@ int choose_bn(int64_t M, int64_t N, int num_sms) {
     return best;
 }
 
+// amax != nullptr: argmax mode (Y unused; the fast path only, else
+// QMM_ERR_UNSUPPORTED); launched the ordinary way.
 qmm_status gemv_impl(int wt, const void *W, size_t w_bytes, int64_t M, int64_t K, const void *X, int xt, int64_t N,
-                     float *Y, void *stream) {
+                     float *Y, void *stream, unsigned long long *amax = nullptr) {
     int E, B;
-    qmm_status s = validate(wt, W, w_bytes, M, K, X, xt, N, Y, QMM_GEMV_MAX_N, E, B);
+    qmm_status s = validate(wt, W, w_bytes, M, K, X, xt, N, amax ? reinterpret_cast<const float *>(amax) : Y,
+                            QMM_GEMV_MAX_N, E, B, amax ? (size_t)N * 8 : 0);
     if (s != QMM_OK) return s;
     DevInfo di;
     if (!dev_info(di)) return QMM_ERR_CUDA;
@@ -220,8 +225,10 @@ qmm_status gemv_impl(int wt, const void *W, size_t w_bytes, int64_t M, int64_t K
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return QMM_ERR_CUDA;
         return from_cuda(launch_gemv_mma(wt, plan, wmap, xmap, X, xt == QMM_X_BF16, M, K, (int)N, Y,
-                                         static_weights(), di.status, g_wait_limit.load(), st));
+                                         amax ? false : static_weights(), di.status, g_wait_limit.load(), st,
+                                         amax));
     }
+    if (amax) return QMM_ERR_UNSUPPORTED;
     return from_cuda(
         launch_gemv_generic(wt, static_cast<const uint8_t *>(W), M, K, X, xt == QMM_X_BF16, (int)N, Y, st));
 }
@@ -325,6 +332,28 @@ size_t qmm_gemm_workspace_bytes(int64_t N, int64_t K, qmm_xtype xt) {
 qmm_status qmm_gemv(qmm_wtype wt, const void *W, size_t w_bytes, int64_t M, int64_t K, const void *X, qmm_xtype xt,
                     int64_t N, float *Y, void *stream) {
     return gemv_impl(wt, W, w_bytes, M, K, X, xt, N, Y, stream);
+}
+
+qmm_status qmm_gemv_argmax(qmm_wtype wt, const void *W, size_t w_bytes, int64_t M, int64_t K, const void *X,
+                           qmm_xtype xt, int64_t N, int32_t *idx, float *val, void *workspace, size_t ws_bytes,
+                           void *stream) {
+    if (!idx || !val || !workspace) return QMM_ERR_INVALID_ARG;
+    if (N < 1 || N > QMM_GEMV_MAX_N || ws_bytes < (size_t)N * 8 || ((uintptr_t)workspace % 8)) return QMM_ERR_INVALID_ARG;
+    if (M > (1ll << 31) - 1) return QMM_ERR_UNSUPPORTED;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    auto *keys = static_cast<unsigned long long *>(workspace);
+    // validate before anything is written (the outputs: idx, val, and the
+    // workspace, none of which may overlap W or X)
+    int E, B;
+    qmm_status s = validate(wt, W, w_bytes, M, K, X, xt, N, val, QMM_GEMV_MAX_N, E, B, (size_t)N * 4);
+    if (s != QMM_OK) return s;
+    s = validate(wt, W, w_bytes, M, K, X, xt, N, reinterpret_cast<const float *>(idx), QMM_GEMV_MAX_N, E, B,
+                 (size_t)N * 4);
+    if (s != QMM_OK) return s;
+    if (cudaMemsetAsync(keys, 0, (size_t)N * 8, st) != cudaSuccess) return QMM_ERR_CUDA;
+    s = gemv_impl(wt, W, w_bytes, M, K, X, xt, N, nullptr, stream, keys);
+    if (s != QMM_OK) return s;
+    return from_cuda(launch_amax_finish(keys, (int)N, idx, val, st));
 }
 
 qmm_status qmm_gemm(qmm_wtype wt, const void *W, size_t w_bytes, int64_t M, int64_t K, const void *X, qmm_xtype xt,

@@ -467,11 +467,67 @@ __device__ __forceinline__ void compute_chunk(float (&acc)[NT][4], const uint8_t
 // one, partials go to shared memory [row][token] and cluster rank 0 sums the
 // KS slices in rank order (deterministic) and stores.
 // ---------------------------------------------------------------------------
+// Order-preserving 64-bit key of (value, row): a larger value wins, then the
+// lower row (the high word maps the float's bits to an unsigned order, the
+// low word holds ~row).  0 is below every key.
+__device__ __forceinline__ unsigned long long amax_key(float v, int row) {
+    const uint32_t u = __float_as_uint(v);
+    const uint32_t o = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return ((unsigned long long)o << 32) | (uint32_t)~(uint32_t)row;
+}
+__device__ __forceinline__ void amax_fold(unsigned long long &best, float v, int row) {
+    const unsigned long long k = amax_key(v, row);
+    best = k > best ? k : best;
+}
+// Maximum over the 8 lanes of a quad column (same t: same tokens, other
+// rows), then one atomic per warp and token.
+__device__ __forceinline__ void amax_commit(unsigned long long *keys, int n, int N, unsigned long long best, int g) {
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+        const unsigned long long x = __shfl_xor_sync(0xffffffffu, best, o);
+        best = x > best ? x : best;
+    }
+    if (g == 0 && n < N && best != 0ull) atomicMax(keys + n, best);
+}
+
 template <int NT, int P, int CW, int RG>
 __device__ __forceinline__ void finish_tile(const float (&acc)[RG][NT][4], float *sred, float *__restrict__ Y, int M,
-                                            int N, int m0, int KS, bool aborted, int warp, int lane) {
+                                            int N, int m0, int KS, bool aborted, int warp, int lane,
+                                            unsigned long long *amax) {
     constexpr int ROWS = 16 * CW * RG;
-    if (KS == 1) {
+    if (KS == 1 && amax) {
+        // argmax mode: Y is not written; each token's best (value, row)
+        if (warp < CW && !aborted) {
+            const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                if constexpr (P == 2) {
+                    const int n = 4 * j + t;
+                    unsigned long long best = 0ull;
+#pragma unroll
+                    for (int q = 0; q < RG; ++q) {
+                        const int r0 = m0 + 16 * (RG * warp + q) + g, r1 = r0 + 8;
+                        if (n < N && r0 < M) amax_fold(best, acc[q][j][0] + acc[q][j][1], r0);
+                        if (n < N && r1 < M) amax_fold(best, acc[q][j][2] + acc[q][j][3], r1);
+                    }
+                    amax_commit(amax, n, N, best, g);
+                } else {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int n = 8 * j + 2 * t + h;
+                        unsigned long long best = 0ull;
+#pragma unroll
+                        for (int q = 0; q < RG; ++q) {
+                            const int r0 = m0 + 16 * (RG * warp + q) + g, r1 = r0 + 8;
+                            if (n < N && r0 < M) amax_fold(best, acc[q][j][h], r0);
+                            if (n < N && r1 < M) amax_fold(best, acc[q][j][2 + h], r1);
+                        }
+                        amax_commit(amax, n, N, best, g);
+                    }
+                }
+            }
+        }
+    } else if (KS == 1) {
         if (warp < CW && !aborted) {
             const int g = lane >> 2, t = lane & 3;
 #pragma unroll
@@ -538,7 +594,12 @@ __device__ __forceinline__ void finish_tile(const float (&acc)[RG][NT][4], float
                 const int row = idx / N, n = idx % N;
                 float v = 0.f;
                 for (int r = 0; r < KS; ++r) v += ld_dsmem_f32(sred + row * 16 + n, (uint32_t)r);
-                if (m0 + row < M && !aborted) Y[(int64_t)n * M + m0 + row] = v;
+                if (m0 + row < M && !aborted) {
+                    if (amax)
+                        atomicMax(amax + n, amax_key(v, m0 + row));
+                    else
+                        Y[(int64_t)n * M + m0 + row] = v;
+                }
             }
         }
         cluster_sync_all();
@@ -548,7 +609,8 @@ __device__ __forceinline__ void finish_tile(const float (&acc)[RG][NT][4], float
 template <int F, int NT, int P, bool XBF16, int CW>
 __global__ void __launch_bounds__(GL<F, NT, CW>::THREADS)
     gemv_mma_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap, int M, int K,
-                    int N, float *__restrict__ Y, int cps, unsigned *status, uint64_t wait_limit) {
+                    int N, float *__restrict__ Y, int cps, unsigned *status, uint64_t wait_limit,
+                    unsigned long long *amax) {
     using L = GL<F, NT, CW>;
     constexpr int S = L::S, XR = L::XR, ROWS = L::ROWS;
     extern __shared__ uint8_t smem_dyn[];
@@ -690,7 +752,7 @@ __global__ void __launch_bounds__(GL<F, NT, CW>::THREADS)
     }
 
     const bool aborted = *abort_flag != 0u;
-    finish_tile<NT, P, CW, 1>(acc, sred, Y, M, N, m0, KS, aborted, warp, lane);
+    finish_tile<NT, P, CW, 1>(acc, sred, Y, M, N, m0, KS, aborted, warp, lane, amax);
     if (threadIdx.x == 0 && aborted) report_status(status, kStatusTimeout);
 }
 
@@ -736,7 +798,8 @@ template <int F, int NC, int CW, int RG> struct GR {
 template <int F, int NC, int P, bool XBF16, int CW, int RG>
 __global__ void __launch_bounds__(GR<F, NC, CW, RG>::THREADS)
     gemv_res_kernel(const __grid_constant__ CUtensorMap wmap, const void *__restrict__ Xv, int M, int K, int N,
-                    float *__restrict__ Y, int cps, unsigned *status, uint64_t wait_limit) {
+                    float *__restrict__ Y, int cps, unsigned *status, uint64_t wait_limit,
+                    unsigned long long *amax) {
     using L = GR<F, NC, CW, RG>;
     constexpr int S = L::S;
     extern __shared__ uint8_t smem_dyn[];
@@ -921,7 +984,7 @@ __global__ void __launch_bounds__(GR<F, NC, CW, RG>::THREADS)
     }
 
     const bool aborted = *abort_flag != 0u;
-    finish_tile<1, P, CW, RG>(acc, sred, Y, M, N, m0, KS, aborted, warp, lane);
+    finish_tile<1, P, CW, RG>(acc, sred, Y, M, N, m0, KS, aborted, warp, lane, amax);
     if (threadIdx.x == 0 && aborted) report_status(status, kStatusTimeout);
 }
 
@@ -944,7 +1007,7 @@ int plan_ks(int64_t tiles, int nchunks, int num_sms, int max_cps, int force) {
 template <typename Kern, typename XArg>
 cudaError_t launch_cluster(Kern kern, int smem, int threads, int64_t tiles, int ks, int nchunks, cudaStream_t st,
                            bool pdl, const CUtensorMap &wmap, const XArg &x_arg, int64_t M, int64_t K, int N,
-                           float *Y, unsigned *status, uint64_t limit) {
+                           float *Y, unsigned *status, uint64_t limit, unsigned long long *amax) {
     const int cps = (nchunks + ks - 1) / ks;
     ks = (nchunks + cps - 1) / cps;   // no empty slices
     int ksp = 1;                      // cluster dims must divide the grid
@@ -970,7 +1033,8 @@ cudaError_t launch_cluster(Kern kern, int smem, int threads, int64_t tiles, int 
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, wmap, x_arg, (int)M, (int)K, N, Y, cps, status, limit);
+    const cudaError_t e =
+        cudaLaunchKernelEx(&cfg, kern, wmap, x_arg, (int)M, (int)K, N, Y, cps, status, limit, amax);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -999,6 +1063,7 @@ struct GemvCall {
     unsigned *status;
     uint64_t limit;
     cudaStream_t st;
+    unsigned long long *amax;   // argmax mode when not null
 };
 
 template <int F, int NT, int P, bool XBF16, int CW>
@@ -1011,7 +1076,7 @@ cudaError_t launch_ring(const GemvCall &c) {
     if (e != cudaSuccess) return e;
     const int64_t tiles = (c.M + L::ROWS - 1) / L::ROWS;
     return launch_cluster(kern, L::SMEM, L::THREADS, tiles, c.plan.ks, (int)(c.K / KC), c.st, c.pdl, *c.wmap,
-                          *c.xmap, c.M, c.K, c.N, c.Y, c.status, c.limit);
+                          *c.xmap, c.M, c.K, c.N, c.Y, c.status, c.limit, c.amax);
 }
 
 template <int F, int NC, int P, bool XBF16, int CW, int RG>
@@ -1026,7 +1091,7 @@ cudaError_t launch_res(const GemvCall &c) {
     if (e != cudaSuccess) return e;
     const int64_t tiles = (c.M + L::ROWS - 1) / L::ROWS;
     return launch_cluster(kern, L::SMEM, L::THREADS, tiles, c.plan.ks, nchunks, c.st, c.pdl, *c.wmap, c.X, c.M,
-                          c.K, c.N, c.Y, c.status, c.limit);
+                          c.K, c.N, c.Y, c.status, c.limit, c.amax);
 }
 
 template <int F, int NC, int P, bool XBF16>
@@ -1110,9 +1175,9 @@ GemvPlan plan_gemv(int64_t M, int64_t K, int N, int xbf16, int num_sms, const Ge
 
 cudaError_t launch_gemv_mma(int fmt, const GemvPlan &plan, const CUtensorMap &wmap, const CUtensorMap &xmap,
                             const void *X, int xbf16, int64_t M, int64_t K, int N, float *Y, bool pdl,
-                            unsigned *status, uint64_t limit, cudaStream_t st) {
+                            unsigned *status, uint64_t limit, cudaStream_t st, unsigned long long *amax) {
     if (N < 1 || N > 16 || plan.ks < 1 || plan.ks > 8) return cudaErrorInvalidValue;
-    const GemvCall c{&wmap, &xmap, X, M, K, N, Y, plan, pdl, status, limit, st};
+    const GemvCall c{&wmap, &xmap, X, M, K, N, Y, plan, pdl, status, limit, st, amax};
     switch (fmt) {
     case Q8_0: return xbf16 ? launch_f<Q8_0, true>(c) : launch_f<Q8_0, false>(c);
     case Q4_0: return xbf16 ? launch_f<Q4_0, true>(c) : launch_f<Q4_0, false>(c);
@@ -1120,6 +1185,22 @@ cudaError_t launch_gemv_mma(int fmt, const GemvPlan &plan, const CUtensorMap &wm
     case Q6_K: return xbf16 ? launch_f<Q6_K, true>(c) : launch_f<Q6_K, false>(c);
     default: return cudaErrorInvalidValue;
     }
+}
+
+__global__ void amax_finish_kernel(const unsigned long long *__restrict__ keys, int N, int32_t *__restrict__ idx,
+                                   float *__restrict__ val) {
+    const int n = threadIdx.x;
+    if (n >= N) return;
+    const unsigned long long k = keys[n];
+    const uint32_t o = (uint32_t)(k >> 32);
+    const uint32_t u = (o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o;   // inverse of the key map
+    idx[n] = (int32_t)~(uint32_t)k;
+    val[n] = __uint_as_float(u);
+}
+
+cudaError_t launch_amax_finish(const unsigned long long *keys, int N, int32_t *idx, float *val, cudaStream_t st) {
+    amax_finish_kernel<<<1, 32, 0, st>>>(keys, N, idx, val);
+    return cudaGetLastError();
 }
 
 }  // namespace qmm

@@ -38,9 +38,15 @@ GemvPlan plan_gemv(int64_t M, int64_t K, int N, int xbf16, int num_sms, const Ge
 // {window/2, plan.rows}; xmap: X [N][K] (f32 or bf16), box {256, N}; X: the
 // same tensor by address.  pdl: launched as a programmatic dependent of the
 // preceding kernel (weights are read before it ends).
+// amax != nullptr: argmax mode; Y is not written and keys[n] (zeroed by the
+// caller) receives the maximum order-preserving key of token n's outputs.
 cudaError_t launch_gemv_mma(int fmt, const GemvPlan &plan, const CUtensorMap &wmap, const CUtensorMap &xmap,
                             const void *X, int xbf16, int64_t M, int64_t K, int N, float *Y, bool pdl,
-                            unsigned *status, uint64_t limit, cudaStream_t st);
+                            unsigned *status, uint64_t limit, cudaStream_t st, unsigned long long *amax = nullptr);
+
+// keys[n] -> idx[n] (row of the largest output, the lowest row on ties),
+// val[n] (that output); N <= 32, one block.
+cudaError_t launch_amax_finish(const unsigned long long *keys, int N, int32_t *idx, float *val, cudaStream_t st);
 
 // Raw bytes of one 256-weight chunk of a row in the GEMV's staging.
 int gemv_window_bytes(int fmt);

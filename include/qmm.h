@@ -107,6 +107,27 @@ QMM_API qmm_status qmm_gemv(qmm_wtype wt, const void *W, size_t w_bytes, int64_t
                     const void *X, qmm_xtype xt, int64_t N, float *Y, void *stream);
 
 /*
+ * Greedy decode through the LM head: for each token n, the row of the
+ * largest output of the GEMV above and that output, without writing the M
+ * outputs anywhere ("cera 0.5.2 src/backend/cpu.rs", gemv_with_preq_argmax;
+ * "cera 0.3.1 src/model/gpu_lfm2.rs", forward_greedy_inner and
+ * encode_argmax_pass, which read back the argmax instead of the logits).
+ * The outputs are computed exactly as qmm_gemv computes them, so idx/val
+ * equal the argmax of qmm_gemv's Y, bit for bit.  Ties go to the lowest row
+ * (the pages' sampler is not on them: reading).
+ *   W, X, N   as for qmm_gemv; the fast path only (16-byte aligned W and X,
+ *             K % 256 == 0, row size a multiple of 16 bytes), else
+ *             QMM_ERR_UNSUPPORTED.
+ *   idx, val  device arrays of N int32 / N float, overwritten.
+ *   workspace device buffer of at least 8 * N bytes, 8-byte aligned (per
+ *             token partial results; contents on return unspecified).
+ * Stream-ordered: a memset of the workspace, the GEMV, a one-block finish.
+ */
+QMM_API qmm_status qmm_gemv_argmax(qmm_wtype wt, const void *W, size_t w_bytes, int64_t M, int64_t K,
+                           const void *X, qmm_xtype xt, int64_t N, int32_t *idx, float *val,
+                           void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * Prefill GEMM on the tensor cores, 1 <= N <= QMM_GEMM_MAX_N
  * ("cera 0.5.0 src/model/llama.rs", forward_prefill_batched and its
  * per-layer projection GEMMs; "cera 0.3.1 src/model/gpu_lfm2.rs",
