@@ -181,14 +181,36 @@ int choose_bn(int64_t M, int64_t N, int num_sms) {
     return best;
 }
 
-// amax != nullptr: argmax mode (Y unused; the fast path only, else
-// QMM_ERR_UNSUPPORTED); launched the ordinary way.
-qmm_status gemv_impl(int wt, const void *W, size_t w_bytes, int64_t M, int64_t K, const void *X, int xt, int64_t N,
-                     float *Y, void *stream, unsigned long long *amax = nullptr) {
-    int E, B;
-    qmm_status s = validate(wt, W, w_bytes, M, K, X, xt, N, amax ? reinterpret_cast<const float *>(amax) : Y,
-                            QMM_GEMV_MAX_N, E, B, amax ? (size_t)N * 8 : 0);
-    if (s != QMM_OK) return s;
+// One GEMV launch over nseg weight matrices of format wt that share X (K,
+// N): fused projections when nseg > 1.  amax != nullptr (nseg == 1): argmax
+// mode (no Y; the fast path only, else QMM_ERR_UNSUPPORTED), launched the
+// ordinary way.
+struct SegIn {
+    const void *W;
+    size_t w_bytes;
+    int64_t M;
+    float *Y;
+};
+
+qmm_status gemv_segments(int wt, const SegIn *seg, int nseg, int64_t K, const void *X, int xt, int64_t N,
+                         void *stream, unsigned long long *amax = nullptr, int32_t *idx = nullptr,
+                         float *val = nullptr) {
+    if (nseg < 1 || nseg > QMM_MAX_SEGS || (amax && nseg != 1)) return QMM_ERR_INVALID_ARG;
+    int E = 0, B = 0;
+    int64_t m_total = 0;
+    for (int i = 0; i < nseg; ++i) {
+        const qmm_status s = validate(wt, seg[i].W, seg[i].w_bytes, seg[i].M, K, X, xt, N,
+                                      amax ? reinterpret_cast<const float *>(amax) : seg[i].Y, QMM_GEMV_MAX_N, E, B,
+                                      amax ? (size_t)(N + 1) * 8 : 0);
+        if (s != QMM_OK) return s;
+        m_total += seg[i].M;
+        for (int j = 0; j < nseg && !amax; ++j) {   // no output may overlap another matrix or output
+            const size_t yi = (size_t)N * (size_t)seg[i].M * 4;
+            if (j != i && (overlaps(seg[i].Y, yi, seg[j].W, (size_t)seg[j].M * (size_t)(K / E) * (size_t)B) ||
+                           overlaps(seg[i].Y, yi, seg[j].Y, (size_t)N * (size_t)seg[j].M * 4)))
+                return QMM_ERR_INVALID_ARG;
+        }
+    }
     DevInfo di;
     if (!dev_info(di)) return QMM_ERR_CUDA;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -196,41 +218,58 @@ qmm_status gemv_impl(int wt, const void *W, size_t w_bytes, int64_t M, int64_t K
     // Tensor-core GEMV: whole 256-weight chunks, TMA-able rows (16-byte
     // aligned base and row pitch), 16-byte aligned X.  Anything else takes the
     // byte-addressed kernel, which computes the same sums.
-    const bool fast = K % 256 == 0 && row_bytes % 16 == 0 && (uintptr_t)W % 16 == 0 && (uintptr_t)X % 16 == 0 &&
-                      M <= (1ll << 31) - 1;
+    bool fast = K % 256 == 0 && row_bytes % 16 == 0 && (uintptr_t)X % 16 == 0 && m_total <= (1ll << 31) - 1;
+    for (int i = 0; i < nseg; ++i) fast = fast && (uintptr_t)seg[i].W % 16 == 0;
     if (fast) {
         EncodeTiledFn enc = encode_fn();
         if (!enc) return QMM_ERR_CUDA;
         const Settings &cfg = settings();
         const GemvTuning tun{cfg.gemv_rows, cfg.gemv_rg, cfg.gemv_ks, cfg.gemv_res};
-        const GemvPlan plan = plan_gemv(M, K, (int)N, xt == QMM_X_BF16, di.num_sms, tun);
-        CUtensorMap wmap;
+        const GemvPlan plan = plan_gemv(m_total, K, (int)N, xt == QMM_X_BF16, di.num_sms, tun);
+        GemvSegs segs{};
+        segs.nseg = nseg;
         const int win = gemv_window_bytes(wt);
-        cuuint64_t dims[2] = {(cuuint64_t)(row_bytes / 2), (cuuint64_t)M};
-        cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
-        cuuint32_t box[2] = {(cuuint32_t)(win / 2), (cuuint32_t)plan.rows};
-        cuuint32_t estr[2] = {1u, 1u};
-        if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void *>(W), dims, strides, box, estr,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return QMM_ERR_CUDA;
+        for (int i = 0; i < nseg; ++i) {
+            cuuint64_t dims[2] = {(cuuint64_t)(row_bytes / 2), (cuuint64_t)seg[i].M};
+            cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+            cuuint32_t box[2] = {(cuuint32_t)(win / 2), (cuuint32_t)plan.rows};
+            cuuint32_t estr[2] = {1u, 1u};
+            if (enc(&segs.wmap[i], CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void *>(seg[i].W), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                return QMM_ERR_CUDA;
+            segs.Y[i] = seg[i].Y;
+            segs.M[i] = (int)seg[i].M;
+        }
         CUtensorMap xmap;
         const int xes = xt == QMM_X_F32 ? 4 : 2;
         cuuint64_t xdims[2] = {(cuuint64_t)K, (cuuint64_t)N};
         cuuint64_t xstrides[1] = {(cuuint64_t)K * xes};
         cuuint32_t xbox[2] = {256u, (cuuint32_t)N};
+        cuuint32_t estr[2] = {1u, 1u};
         if (enc(&xmap, xt == QMM_X_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
                 const_cast<void *>(X), xdims, xstrides, xbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                 CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return QMM_ERR_CUDA;
-        return from_cuda(launch_gemv_mma(wt, plan, wmap, xmap, X, xt == QMM_X_BF16, M, K, (int)N, Y,
-                                         amax ? false : static_weights(), di.status, g_wait_limit.load(), st,
-                                         amax));
+        return from_cuda(launch_gemv_mma(wt, plan, segs, xmap, X, xt == QMM_X_BF16, K, (int)N,
+                                         amax ? false : static_weights(), di.status, g_wait_limit.load(), st, amax,
+                                         idx, val));
     }
     if (amax) return QMM_ERR_UNSUPPORTED;
-    return from_cuda(
-        launch_gemv_generic(wt, static_cast<const uint8_t *>(W), M, K, X, xt == QMM_X_BF16, (int)N, Y, st));
+    for (int i = 0; i < nseg; ++i) {
+        const qmm_status s = from_cuda(launch_gemv_generic(wt, static_cast<const uint8_t *>(seg[i].W), seg[i].M, K, X,
+                                                           xt == QMM_X_BF16, (int)N, seg[i].Y, st));
+        if (s != QMM_OK) return s;
+    }
+    return QMM_OK;
+}
+
+qmm_status gemv_impl(int wt, const void *W, size_t w_bytes, int64_t M, int64_t K, const void *X, int xt, int64_t N,
+                     float *Y, void *stream, unsigned long long *amax = nullptr, int32_t *idx = nullptr,
+                     float *val = nullptr) {
+    const SegIn seg{W, w_bytes, M, Y};
+    return gemv_segments(wt, &seg, 1, K, X, xt, N, stream, amax, idx, val);
 }
 
 qmm_status gemm_impl(int wt, const void *W, size_t w_bytes, int64_t M, int64_t K, const void *X, int xt, int64_t N,
@@ -334,11 +373,22 @@ qmm_status qmm_gemv(qmm_wtype wt, const void *W, size_t w_bytes, int64_t M, int6
     return gemv_impl(wt, W, w_bytes, M, K, X, xt, N, Y, stream);
 }
 
+static_assert(QMM_MAX_MATRICES == QMM_MAX_SEGS, "one launch holds every matrix of a fused call");
+
+qmm_status qmm_gemv_multi(qmm_wtype wt, const qmm_matrix *mats, int nmat, int64_t K, const void *X, qmm_xtype xt,
+                          int64_t N, void *stream) {
+    if (!mats || nmat < 1 || nmat > QMM_MAX_MATRICES) return QMM_ERR_INVALID_ARG;
+    SegIn seg[QMM_MAX_MATRICES];
+    for (int i = 0; i < nmat; ++i) seg[i] = SegIn{mats[i].W, mats[i].w_bytes, mats[i].M, mats[i].Y};
+    return gemv_segments(wt, seg, nmat, K, X, xt, N, stream);
+}
+
 qmm_status qmm_gemv_argmax(qmm_wtype wt, const void *W, size_t w_bytes, int64_t M, int64_t K, const void *X,
                            qmm_xtype xt, int64_t N, int32_t *idx, float *val, void *workspace, size_t ws_bytes,
                            void *stream) {
     if (!idx || !val || !workspace) return QMM_ERR_INVALID_ARG;
-    if (N < 1 || N > QMM_GEMV_MAX_N || ws_bytes < (size_t)N * 8 || ((uintptr_t)workspace % 8)) return QMM_ERR_INVALID_ARG;
+    if (N < 1 || N > QMM_GEMV_MAX_N || ws_bytes < (size_t)(N + 1) * 8 || ((uintptr_t)workspace % 8))
+        return QMM_ERR_INVALID_ARG;
     if (M > (1ll << 31) - 1) return QMM_ERR_UNSUPPORTED;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     auto *keys = static_cast<unsigned long long *>(workspace);
@@ -350,10 +400,8 @@ qmm_status qmm_gemv_argmax(qmm_wtype wt, const void *W, size_t w_bytes, int64_t 
     s = validate(wt, W, w_bytes, M, K, X, xt, N, reinterpret_cast<const float *>(idx), QMM_GEMV_MAX_N, E, B,
                  (size_t)N * 4);
     if (s != QMM_OK) return s;
-    if (cudaMemsetAsync(keys, 0, (size_t)N * 8, st) != cudaSuccess) return QMM_ERR_CUDA;
-    s = gemv_impl(wt, W, w_bytes, M, K, X, xt, N, nullptr, stream, keys);
-    if (s != QMM_OK) return s;
-    return from_cuda(launch_amax_finish(keys, (int)N, idx, val, st));
+    if (cudaMemsetAsync(keys, 0, (size_t)(N + 1) * 8, st) != cudaSuccess) return QMM_ERR_CUDA;   // keys + counter
+    return gemv_impl(wt, W, w_bytes, M, K, X, xt, N, nullptr, stream, keys, idx, val);
 }
 
 qmm_status qmm_gemm(qmm_wtype wt, const void *W, size_t w_bytes, int64_t M, int64_t K, const void *X, qmm_xtype xt,

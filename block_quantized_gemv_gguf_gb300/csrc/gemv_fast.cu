@@ -467,6 +467,15 @@ __device__ __forceinline__ void compute_chunk(float (&acc)[NT][4], const uint8_t
 // one, partials go to shared memory [row][token] and cluster rank 0 sums the
 // KS slices in rank order (deterministic) and stores.
 // ---------------------------------------------------------------------------
+// Argmax-mode outputs: per-token keys (zeroed by the host with the counter),
+// a counter of finished CTAs, and the unpacked results the last CTA writes.
+struct AmaxOut {
+    unsigned long long *keys;   // null: ordinary GEMV
+    unsigned *counter;
+    int32_t *idx;
+    float *val;
+};
+
 // Order-preserving 64-bit key of (value, row): a larger value wins, then the
 // lower row (the high word maps the float's bits to an unsigned order, the
 // low word holds ~row).  0 is below every key.
@@ -488,6 +497,28 @@ __device__ __forceinline__ void amax_commit(unsigned long long *keys, int n, int
         best = x > best ? x : best;
     }
     if (g == 0 && n < N && best != 0ull) atomicMax(keys + n, best);
+}
+
+// Argmax mode, after every CTA's keys are in: the last CTA to finish (a
+// fenced counter) unpacks keys[n] into idx[n] (row) and val[n] (output).
+__device__ __forceinline__ void amax_last_cta(const AmaxOut &a, int N) {
+    __shared__ unsigned s_last;
+    if (!a.keys) return;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const unsigned done = atomicAdd(a.counter, 1u);
+        s_last = done == gridDim.x * gridDim.y - 1 ? 1u : 0u;
+    }
+    __syncthreads();
+    if (s_last && (int)threadIdx.x < N) {
+        __threadfence();
+        const unsigned long long k = atomicAdd(a.keys + threadIdx.x, 0ull);   // coherent read
+        const uint32_t o = (uint32_t)(k >> 32);
+        const uint32_t u = (o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o;       // inverse of the key map
+        a.idx[threadIdx.x] = (int32_t)~(uint32_t)k;
+        a.val[threadIdx.x] = __uint_as_float(u);
+    }
 }
 
 template <int NT, int P, int CW, int RG>
@@ -608,9 +639,8 @@ __device__ __forceinline__ void finish_tile(const float (&acc)[RG][NT][4], float
 
 template <int F, int NT, int P, bool XBF16, int CW>
 __global__ void __launch_bounds__(GL<F, NT, CW>::THREADS)
-    gemv_mma_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap, int M, int K,
-                    int N, float *__restrict__ Y, int cps, unsigned *status, uint64_t wait_limit,
-                    unsigned long long *amax) {
+    gemv_mma_kernel(const __grid_constant__ GemvSegs segs, const __grid_constant__ CUtensorMap xmap, int K, int N,
+                    int cps, unsigned *status, uint64_t wait_limit, AmaxOut amax) {
     using L = GL<F, NT, CW>;
     constexpr int S = L::S, XR = L::XR, ROWS = L::ROWS;
     extern __shared__ uint8_t smem_dyn[];
@@ -631,7 +661,13 @@ __global__ void __launch_bounds__(GL<F, NT, CW>::THREADS)
     volatile unsigned *abort_flag = reinterpret_cast<volatile unsigned *>(smem + L::OFF_MISC);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.x * ROWS;
+    // this CTA's weight matrix (segment) and tile within it
+    int sg = 0;
+    while (sg + 1 < segs.nseg && (int)blockIdx.x >= segs.tile0[sg + 1]) ++sg;
+    const CUtensorMap *wmap = &segs.wmap[sg];
+    const int M = segs.M[sg];
+    float *__restrict__ Y = segs.Y[sg];
+    const int m0 = ((int)blockIdx.x - segs.tile0[sg]) * ROWS;
     const int nchunks = K / KC;
     const int c_begin = blockIdx.y * cps;
     const int c_end = min(nchunks, c_begin + cps);
@@ -666,7 +702,7 @@ __global__ void __launch_bounds__(GL<F, NT, CW>::THREADS)
         // ---------------- TMA producers: lane 0 weights, lane 1 raw X ----------------
         const uint64_t drain_limit = wait_limit < (1ull << 31) ? (1ull << 31) : wait_limit;
         if (lane == 0) {
-            prefetch_tensormap(&wmap);
+            prefetch_tensormap(wmap);
             int issued = 0;   // loads are issued in chunk order 0, 1, ..., issued-1
             for (int c = 0; c < nloc; ++c) {
                 const int s = c % S;
@@ -675,7 +711,7 @@ __global__ void __launch_bounds__(GL<F, NT, CW>::THREADS)
                 const int cg = c_begin + c;
                 const int xb = F == Q6_K ? ((210 * cg) & ~15) : cg * L::WIN;
                 mbar_arrive_expect_tx(&full[s], (uint32_t)L::RAWW);
-                tma_load_2d(sstage + s * L::STAGE, &wmap, &full[s], xb >> 1, m0);
+                tma_load_2d(sstage + s * L::STAGE, wmap, &full[s], xb >> 1, m0);
                 issued = c + 1;
             }
             if (*abort_flag)   // drain: the last load issued into each stage
@@ -752,7 +788,8 @@ __global__ void __launch_bounds__(GL<F, NT, CW>::THREADS)
     }
 
     const bool aborted = *abort_flag != 0u;
-    finish_tile<NT, P, CW, 1>(acc, sred, Y, M, N, m0, KS, aborted, warp, lane, amax);
+    finish_tile<NT, P, CW, 1>(acc, sred, Y, M, N, m0, KS, aborted, warp, lane, amax.keys);
+    amax_last_cta(amax, N);
     if (threadIdx.x == 0 && aborted) report_status(status, kStatusTimeout);
 }
 
@@ -797,9 +834,8 @@ template <int F, int NC, int CW, int RG> struct GR {
 
 template <int F, int NC, int P, bool XBF16, int CW, int RG>
 __global__ void __launch_bounds__(GR<F, NC, CW, RG>::THREADS)
-    gemv_res_kernel(const __grid_constant__ CUtensorMap wmap, const void *__restrict__ Xv, int M, int K, int N,
-                    float *__restrict__ Y, int cps, unsigned *status, uint64_t wait_limit,
-                    unsigned long long *amax) {
+    gemv_res_kernel(const __grid_constant__ GemvSegs segs, const void *__restrict__ Xv, int K, int N, int cps,
+                    unsigned *status, uint64_t wait_limit, AmaxOut amax) {
     using L = GR<F, NC, CW, RG>;
     constexpr int S = L::S;
     extern __shared__ uint8_t smem_dyn[];
@@ -817,7 +853,13 @@ __global__ void __launch_bounds__(GR<F, NC, CW, RG>::THREADS)
     volatile unsigned *abort_flag = reinterpret_cast<volatile unsigned *>(smem + L::OFF_MISC);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.x * L::ROWS;
+    // this CTA's weight matrix (segment) and tile within it
+    int sg = 0;
+    while (sg + 1 < segs.nseg && (int)blockIdx.x >= segs.tile0[sg + 1]) ++sg;
+    const CUtensorMap *wmap = &segs.wmap[sg];
+    const int M = segs.M[sg];
+    float *__restrict__ Y = segs.Y[sg];
+    const int m0 = ((int)blockIdx.x - segs.tile0[sg]) * L::ROWS;
     const int nchunks = K / KC;
     const int c_begin = blockIdx.y * cps;
     const int c_end = min(nchunks, c_begin + cps);
@@ -844,7 +886,7 @@ __global__ void __launch_bounds__(GR<F, NC, CW, RG>::THREADS)
     if (warp == L::WARP_TMA) {
         if (lane == 0) {
             const uint64_t drain_limit = wait_limit < (1ull << 31) ? (1ull << 31) : wait_limit;
-            prefetch_tensormap(&wmap);
+            prefetch_tensormap(wmap);
             int issued = 0;
             bool x_issued = false;
             for (int c = 0; c < nloc; ++c) {
@@ -854,7 +896,7 @@ __global__ void __launch_bounds__(GR<F, NC, CW, RG>::THREADS)
                 const int cg = c_begin + c;
                 const int xb = F == Q6_K ? ((210 * cg) & ~15) : cg * L::WIN;
                 mbar_arrive_expect_tx(&full[s], (uint32_t)L::STAGE);
-                tma_load_2d(sstage + s * L::STAGE, &wmap, &full[s], xb >> 1, m0);
+                tma_load_2d(sstage + s * L::STAGE, wmap, &full[s], xb >> 1, m0);
                 issued = c + 1;
                 if (c == (nloc < S ? nloc : S) - 1) {
                     // Weights are read before the preceding kernel on the
@@ -984,7 +1026,8 @@ __global__ void __launch_bounds__(GR<F, NC, CW, RG>::THREADS)
     }
 
     const bool aborted = *abort_flag != 0u;
-    finish_tile<1, P, CW, RG>(acc, sred, Y, M, N, m0, KS, aborted, warp, lane, amax);
+    finish_tile<1, P, CW, RG>(acc, sred, Y, M, N, m0, KS, aborted, warp, lane, amax.keys);
+    amax_last_cta(amax, N);
     if (threadIdx.x == 0 && aborted) report_status(status, kStatusTimeout);
 }
 
@@ -1006,8 +1049,8 @@ int plan_ks(int64_t tiles, int nchunks, int num_sms, int max_cps, int force) {
 // x_arg: the kernel's second parameter (X tensor map or X address).
 template <typename Kern, typename XArg>
 cudaError_t launch_cluster(Kern kern, int smem, int threads, int64_t tiles, int ks, int nchunks, cudaStream_t st,
-                           bool pdl, const CUtensorMap &wmap, const XArg &x_arg, int64_t M, int64_t K, int N,
-                           float *Y, unsigned *status, uint64_t limit, unsigned long long *amax) {
+                           bool pdl, const GemvSegs &segs, const XArg &x_arg, int64_t K, int N, unsigned *status,
+                           uint64_t limit, const AmaxOut &amax) {
     const int cps = (nchunks + ks - 1) / ks;
     ks = (nchunks + cps - 1) / cps;   // no empty slices
     int ksp = 1;                      // cluster dims must divide the grid
@@ -1034,7 +1077,7 @@ cudaError_t launch_cluster(Kern kern, int smem, int threads, int64_t tiles, int 
     cfg.attrs = attr;
     cfg.numAttrs = na;
     const cudaError_t e =
-        cudaLaunchKernelEx(&cfg, kern, wmap, x_arg, (int)M, (int)K, N, Y, cps, status, limit, amax);
+        cudaLaunchKernelEx(&cfg, kern, segs, x_arg, (int)K, N, cps, status, limit, amax);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -1053,18 +1096,29 @@ cudaError_t set_smem_once(Kern kern, int smem, std::atomic<uint64_t> &configured
 }
 
 struct GemvCall {
-    const CUtensorMap *wmap, *xmap;
+    const GemvSegs *segs;
+    const CUtensorMap *xmap;
     const void *X;
-    int64_t M, K;
+    int64_t K;
     int N;
-    float *Y;
     GemvPlan plan;
     bool pdl;
     unsigned *status;
     uint64_t limit;
     cudaStream_t st;
-    unsigned long long *amax;   // argmax mode when not null
+    AmaxOut amax;               // argmax mode when amax.keys is not null
 };
+
+// First tile of every segment (tile0[nseg] = all tiles) for `rows`-row tiles.
+int64_t set_tiles(GemvSegs &sg, int rows) {
+    int64_t t = 0;
+    for (int i = 0; i < sg.nseg; ++i) {
+        sg.tile0[i] = (int)t;
+        t += (sg.M[i] + rows - 1) / rows;
+    }
+    sg.tile0[sg.nseg] = (int)t;
+    return t;
+}
 
 template <int F, int NT, int P, bool XBF16, int CW>
 cudaError_t launch_ring(const GemvCall &c) {
@@ -1074,9 +1128,10 @@ cudaError_t launch_ring(const GemvCall &c) {
     static std::atomic<uint64_t> configured{0};
     cudaError_t e = set_smem_once(kern, L::SMEM, configured);
     if (e != cudaSuccess) return e;
-    const int64_t tiles = (c.M + L::ROWS - 1) / L::ROWS;
-    return launch_cluster(kern, L::SMEM, L::THREADS, tiles, c.plan.ks, (int)(c.K / KC), c.st, c.pdl, *c.wmap,
-                          *c.xmap, c.M, c.K, c.N, c.Y, c.status, c.limit, c.amax);
+    GemvSegs sg = *c.segs;
+    const int64_t tiles = set_tiles(sg, L::ROWS);
+    return launch_cluster(kern, L::SMEM, L::THREADS, tiles, c.plan.ks, (int)(c.K / KC), c.st, c.pdl, sg, *c.xmap, c.K,
+                          c.N, c.status, c.limit, c.amax);
 }
 
 template <int F, int NC, int P, bool XBF16, int CW, int RG>
@@ -1089,9 +1144,10 @@ cudaError_t launch_res(const GemvCall &c) {
     static std::atomic<uint64_t> configured{0};
     cudaError_t e = set_smem_once(kern, L::SMEM, configured);
     if (e != cudaSuccess) return e;
-    const int64_t tiles = (c.M + L::ROWS - 1) / L::ROWS;
-    return launch_cluster(kern, L::SMEM, L::THREADS, tiles, c.plan.ks, nchunks, c.st, c.pdl, *c.wmap, c.X, c.M,
-                          c.K, c.N, c.Y, c.status, c.limit, c.amax);
+    GemvSegs sg = *c.segs;
+    const int64_t tiles = set_tiles(sg, L::ROWS);
+    return launch_cluster(kern, L::SMEM, L::THREADS, tiles, c.plan.ks, nchunks, c.st, c.pdl, sg, c.X, c.K, c.N,
+                          c.status, c.limit, c.amax);
 }
 
 template <int F, int NC, int P, bool XBF16>
@@ -1173,11 +1229,13 @@ GemvPlan plan_gemv(int64_t M, int64_t K, int N, int xbf16, int num_sms, const Ge
     return p;
 }
 
-cudaError_t launch_gemv_mma(int fmt, const GemvPlan &plan, const CUtensorMap &wmap, const CUtensorMap &xmap,
-                            const void *X, int xbf16, int64_t M, int64_t K, int N, float *Y, bool pdl,
-                            unsigned *status, uint64_t limit, cudaStream_t st, unsigned long long *amax) {
+cudaError_t launch_gemv_mma(int fmt, const GemvPlan &plan, const GemvSegs &segs, const CUtensorMap &xmap,
+                            const void *X, int xbf16, int64_t K, int N, bool pdl, unsigned *status, uint64_t limit,
+                            cudaStream_t st, unsigned long long *amax_ws, int32_t *idx, float *val) {
     if (N < 1 || N > 16 || plan.ks < 1 || plan.ks > 8) return cudaErrorInvalidValue;
-    const GemvCall c{&wmap, &xmap, X, M, K, N, Y, plan, pdl, status, limit, st, amax};
+    if (segs.nseg < 1 || segs.nseg > QMM_MAX_SEGS || (amax_ws && segs.nseg != 1)) return cudaErrorInvalidValue;
+    const AmaxOut amax{amax_ws, amax_ws ? reinterpret_cast<unsigned *>(amax_ws + N) : nullptr, idx, val};
+    const GemvCall c{&segs, &xmap, X, K, N, plan, pdl, status, limit, st, amax};
     switch (fmt) {
     case Q8_0: return xbf16 ? launch_f<Q8_0, true>(c) : launch_f<Q8_0, false>(c);
     case Q4_0: return xbf16 ? launch_f<Q4_0, true>(c) : launch_f<Q4_0, false>(c);
@@ -1185,22 +1243,6 @@ cudaError_t launch_gemv_mma(int fmt, const GemvPlan &plan, const CUtensorMap &wm
     case Q6_K: return xbf16 ? launch_f<Q6_K, true>(c) : launch_f<Q6_K, false>(c);
     default: return cudaErrorInvalidValue;
     }
-}
-
-__global__ void amax_finish_kernel(const unsigned long long *__restrict__ keys, int N, int32_t *__restrict__ idx,
-                                   float *__restrict__ val) {
-    const int n = threadIdx.x;
-    if (n >= N) return;
-    const unsigned long long k = keys[n];
-    const uint32_t o = (uint32_t)(k >> 32);
-    const uint32_t u = (o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o;   // inverse of the key map
-    idx[n] = (int32_t)~(uint32_t)k;
-    val[n] = __uint_as_float(u);
-}
-
-cudaError_t launch_amax_finish(const unsigned long long *keys, int N, int32_t *idx, float *val, cudaStream_t st) {
-    amax_finish_kernel<<<1, 32, 0, st>>>(keys, N, idx, val);
-    return cudaGetLastError();
 }
 
 }  // namespace qmm

@@ -33,20 +33,30 @@ struct GemvPlan {
 };
 GemvPlan plan_gemv(int64_t M, int64_t K, int N, int xbf16, int num_sms, const GemvTuning &tun);
 
-// Tensor-core GEMV, 1 <= N <= 16 (K % 256 == 0, 16-byte aligned W rows and
-// X), executing `plan`.  wmap: raw weight bytes as u16 [M][row_bytes/2], box
-// {window/2, plan.rows}; xmap: X [N][K] (f32 or bf16), box {256, N}; X: the
-// same tensor by address.  pdl: launched as a programmatic dependent of the
-// preceding kernel (weights are read before it ends).
-// amax != nullptr: argmax mode; Y is not written and keys[n] (zeroed by the
-// caller) receives the maximum order-preserving key of token n's outputs.
-cudaError_t launch_gemv_mma(int fmt, const GemvPlan &plan, const CUtensorMap &wmap, const CUtensorMap &xmap,
-                            const void *X, int xbf16, int64_t M, int64_t K, int N, float *Y, bool pdl,
-                            unsigned *status, uint64_t limit, cudaStream_t st, unsigned long long *amax = nullptr);
+// Weight matrices of one GEMV launch (several share X: fused projections).
+// The host fills wmap (box {window/2, plan.rows}), Y and M per matrix; the
+// launcher fills tile0.
+constexpr int QMM_MAX_SEGS = 4;
+struct GemvSegs {
+    CUtensorMap wmap[QMM_MAX_SEGS];
+    float *Y[QMM_MAX_SEGS];
+    int M[QMM_MAX_SEGS];
+    int tile0[QMM_MAX_SEGS + 1];   // first tile of each matrix; [nseg] = all tiles
+    int nseg;
+};
 
-// keys[n] -> idx[n] (row of the largest output, the lowest row on ties),
-// val[n] (that output); N <= 32, one block.
-cudaError_t launch_amax_finish(const unsigned long long *keys, int N, int32_t *idx, float *val, cudaStream_t st);
+// Tensor-core GEMV, 1 <= N <= 16 (K % 256 == 0, 16-byte aligned W rows and
+// X), executing `plan` over every matrix of `segs`.  xmap: X [N][K] (f32 or
+// bf16), box {256, N}; X: the same tensor by address.  pdl: launched as a
+// programmatic dependent of the preceding kernel (weights are read before it
+// ends).  amax_ws != nullptr (one matrix only): argmax mode.  Y is not
+// written; amax_ws holds N keys and a finished-CTA counter (zeroed by the
+// caller, 8 * (N + 1) bytes), and the last CTA writes idx[n] (row of token
+// n's largest output, the lowest row on ties) and val[n] (that output).
+cudaError_t launch_gemv_mma(int fmt, const GemvPlan &plan, const GemvSegs &segs, const CUtensorMap &xmap,
+                            const void *X, int xbf16, int64_t K, int N, bool pdl, unsigned *status, uint64_t limit,
+                            cudaStream_t st, unsigned long long *amax_ws = nullptr, int32_t *idx = nullptr,
+                            float *val = nullptr);
 
 // Raw bytes of one 256-weight chunk of a row in the GEMV's staging.
 int gemv_window_bytes(int fmt);

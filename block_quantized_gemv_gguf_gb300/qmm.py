@@ -25,7 +25,7 @@ X_F32, X_BF16 = 0, 1
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = 0, 1, 2, 3, 4
 GEMV_MAX_N, GEMM_MAX_N = 16, 512
 BLOCK = {Q8_0: (32, 34), Q4_0: (32, 18), Q4_K: (256, 144), Q6_K: (256, 210)}
-EXPORTS = ("qmm_gemv", "qmm_gemv_argmax", "qmm_gemm", "qmm_gemm_workspace_bytes", "qmm_matmul", "qmm_matmul_host",
+EXPORTS = ("qmm_gemv", "qmm_gemv_argmax", "qmm_gemv_multi", "qmm_gemm", "qmm_gemm_workspace_bytes", "qmm_matmul", "qmm_matmul_host",
            "qmm_dequant", "qmm_block_info", "qmm_last_device_error", "qmm_status_str",
            "qmm_set_wait_limit", "qmm_set_static_weights")
 
@@ -55,6 +55,7 @@ def load() -> ctypes.CDLL:
         i64, sz, p, ci = ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_int
         lib.qmm_gemv.argtypes = [ci, p, sz, i64, i64, p, ci, i64, p, p]
         lib.qmm_gemv_argmax.argtypes = [ci, p, sz, i64, i64, p, ci, i64, p, p, p, sz, p]
+        lib.qmm_gemv_multi.argtypes = [ci, p, ci, i64, p, ci, i64, p]
         lib.qmm_gemm.argtypes = [ci, p, sz, i64, i64, p, ci, i64, p, p, sz, p]
         lib.qmm_matmul.argtypes = [ci, p, sz, i64, i64, p, ci, i64, p, p, sz, p]
         lib.qmm_matmul_host.argtypes = [ci, p, sz, i64, i64, p, ci, i64, p, p, p, p, sz, p]
@@ -69,7 +70,7 @@ def load() -> ctypes.CDLL:
         lib.qmm_set_wait_limit.restype = None
         lib.qmm_set_static_weights.argtypes = [ctypes.c_int]
         lib.qmm_set_static_weights.restype = None
-        for f in ("qmm_gemv", "qmm_gemv_argmax", "qmm_gemm", "qmm_matmul", "qmm_matmul_host", "qmm_dequant", "qmm_block_info",
+        for f in ("qmm_gemv", "qmm_gemv_argmax", "qmm_gemv_multi", "qmm_gemm", "qmm_matmul", "qmm_matmul_host", "qmm_dequant", "qmm_block_info",
                   "qmm_last_device_error"):
             getattr(lib, f).restype = ci
         _lib = lib
@@ -122,13 +123,32 @@ def qmm_gemv_argmax(wt, W, M, K, X, N, idx, val, workspace, stream=None, w_bytes
                                   _nbytes(workspace), _stream(stream))
 
 
+class QmmMatrix(ctypes.Structure):
+    _fields_ = [("W", ctypes.c_void_p), ("w_bytes", ctypes.c_size_t), ("M", ctypes.c_int64), ("Y", ctypes.c_void_p)]
+
+
+def qmm_gemv_multi(wt, mats, K, X, N, stream=None, xt=None) -> int:
+    """mats: list of (W, M, Y) sharing X; one launch."""
+    arr = (QmmMatrix * len(mats))(*[QmmMatrix(_ptr(W), _nbytes(W), M, _ptr(Y)) for (W, M, Y) in mats])
+    return load().qmm_gemv_multi(wt, ctypes.cast(arr, ctypes.c_void_p), len(mats), K, _ptr(X),
+                                 _xtype(X) if xt is None else xt, N, _stream(stream))
+
+
+def gemv_multi(wt, Ws_and_Ms, K, X, stream=None):
+    """[Y_i [N, M_i]] for [(W_i, M_i)] sharing X, in one launch."""
+    N = _shape(X, K)
+    Ys = [torch.empty(N, M, dtype=torch.float32, device=X.device) for (_, M) in Ws_and_Ms]
+    _check(qmm_gemv_multi(wt, [(W, M, Y) for (W, M), Y in zip(Ws_and_Ms, Ys)], K, X, N, stream), "qmm_gemv_multi")
+    return Ys
+
+
 def gemv_argmax(wt, W, M, K, X, stream=None):
     """(idx int32 [N], val float32 [N]): per token, the row of the largest
     GEMV output and that output, without materializing the outputs."""
     N = _shape(X, K)
     idx = torch.empty(N, dtype=torch.int32, device=X.device)
     val = torch.empty(N, dtype=torch.float32, device=X.device)
-    ws = torch.empty(N, dtype=torch.int64, device=X.device)
+    ws = torch.empty(N + 1, dtype=torch.int64, device=X.device)
     _check(qmm_gemv_argmax(wt, W, M, K, X, N, idx, val, ws, stream), "qmm_gemv_argmax")
     return idx, val
 

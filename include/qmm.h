@@ -107,6 +107,30 @@ QMM_API qmm_status qmm_gemv(qmm_wtype wt, const void *W, size_t w_bytes, int64_t
                     const void *X, qmm_xtype xt, int64_t N, float *Y, void *stream);
 
 /*
+ * Fused projections: up to QMM_MAX_MATRICES weight matrices of one format
+ * that share X (Q/K/V of an attention layer, gate and up of a feed-forward
+ * layer), in one launch: Y_i[N, M_i] = X[N, K] . dequant(W_i)[M_i, K]^T
+ * ("cera 0.5.2 src/backend/cpu.rs", gemv_q4_0_fused2_with_q8 and
+ * gemv_q4_0_concat3_with_q8: several matrices, one pass over a shared x).
+ * Every output meets the qmm_gemv bound against exact arithmetic (the K
+ * split, and so the f32 summation order, follows the total row count).
+ *   mats[i]   W (raw blocks), w_bytes, M (rows) and Y ([N, M] f32,
+ *             overwritten) of matrix i; no Y may overlap any W, X or other Y.
+ *   K, X, xt, N   as for qmm_gemv, shared.
+ * The fast path needs every W 16-byte aligned (and the conditions of
+ * qmm_gemv); otherwise each matrix runs the byte-addressed path.
+ */
+#define QMM_MAX_MATRICES 4
+typedef struct {
+    const void *W;
+    size_t w_bytes;
+    int64_t M;
+    float *Y;
+} qmm_matrix;
+QMM_API qmm_status qmm_gemv_multi(qmm_wtype wt, const qmm_matrix *mats, int nmat, int64_t K, const void *X,
+                          qmm_xtype xt, int64_t N, void *stream);
+
+/*
  * Greedy decode through the LM head: for each token n, the row of the
  * largest output of the GEMV above and that output, without writing the M
  * outputs anywhere ("cera 0.5.2 src/backend/cpu.rs", gemv_with_preq_argmax;
@@ -119,9 +143,11 @@ QMM_API qmm_status qmm_gemv(qmm_wtype wt, const void *W, size_t w_bytes, int64_t
  *             K % 256 == 0, row size a multiple of 16 bytes), else
  *             QMM_ERR_UNSUPPORTED.
  *   idx, val  device arrays of N int32 / N float, overwritten.
- *   workspace device buffer of at least 8 * N bytes, 8-byte aligned (per
- *             token partial results; contents on return unspecified).
- * Stream-ordered: a memset of the workspace, the GEMV, a one-block finish.
+ *   workspace device buffer of at least 8 * (N + 1) bytes, 8-byte aligned
+ *             (per-token partial results and a counter; contents on return
+ *             unspecified).
+ * Stream-ordered: a memset of the workspace, then the GEMV, whose last CTA
+ * writes idx and val.
  */
 QMM_API qmm_status qmm_gemv_argmax(qmm_wtype wt, const void *W, size_t w_bytes, int64_t M, int64_t K,
                            const void *X, qmm_xtype xt, int64_t N, int32_t *idx, float *val,

@@ -103,8 +103,8 @@ def test_argmax_errors():
     X = torch.from_numpy(synth.gen_x(N, K, "amax-err")).cuda()
     idx = torch.empty(N, dtype=torch.int32, device="cuda")
     val = torch.empty(N, device="cuda")
-    ws = torch.empty(N, dtype=torch.int64, device="cuda")
-    assert qmm.qmm_gemv_argmax(wt, W, M, K, X, N, idx, val, ws[:1]) == qmm.ERR_INVALID_ARG   # workspace too small
+    ws = torch.empty(N + 1, dtype=torch.int64, device="cuda")
+    assert qmm.qmm_gemv_argmax(wt, W, M, K, X, N, idx, val, ws[:N]) == qmm.ERR_INVALID_ARG   # workspace too small
     assert qmm.qmm_gemv_argmax(wt, W, M, K, X, 17, idx, val, ws) == qmm.ERR_INVALID_ARG      # N > 16
     base = torch.zeros(W.numel() + 16, dtype=torch.uint8, device="cuda")
     base[1:1 + W.numel()] = W
@@ -119,12 +119,12 @@ def test_argmax_small_outputs_next_to_inputs():
     w = synth.gen_weights(wt, M, K, "amax-adj")
     x = synth.gen_x(N, K, "amax-adj")
     W = torch.from_numpy(w).cuda()
-    buf = torch.empty(N * K + 64, dtype=torch.float32, device="cuda")
+    buf = torch.empty(N * K + 64, dtype=torch.float32, device="cuda")   # X, then val, idx, workspace
     X = buf[:N * K].view(N, K)
     X.copy_(torch.from_numpy(x).cuda())
     val = buf[N * K:N * K + N]
     idx = buf[N * K + 16:N * K + 16 + N].view(torch.int32)
-    ws = buf[N * K + 32:N * K + 32 + 2 * N].view(torch.int64)
+    ws = buf[N * K + 32:N * K + 32 + 2 * (N + 1)].view(torch.int64)
     assert qmm.qmm_gemv_argmax(wt, W, M, K, X, N, idx, val, ws) == qmm.OK
     y = qmm.gemv(wt, W, M, K, X)
     torch.cuda.synchronize()
