@@ -70,6 +70,10 @@ def _load():
             lib.orc_dequant_f32.argtypes = [ctypes.c_int, p, i64, i64, p]
             lib.orc_matmul_rows.argtypes = [ctypes.c_int, p, i64, i64, p, ctypes.c_int, i64,
                                             p, i64, p, p, ctypes.c_int]
+            lib.orc_f32_to_f16.argtypes = [ctypes.c_float]
+            lib.orc_f32_to_f16.restype = ctypes.c_uint16
+            lib.orc_quantize_q8_0.argtypes = [p, i64, p, p]
+            lib.orc_quantize_q8_0.restype = ctypes.c_int
             for f in (lib.orc_dequant_block, lib.orc_dequant, lib.orc_dequant_f32, lib.orc_matmul_rows):
                 f.restype = ctypes.c_int
             _lib = lib
@@ -148,6 +152,40 @@ def matmul(wtype: int, w: np.ndarray, M: int, K: int, x: np.ndarray, rows=None,
                                _ptr(Y), _ptr(S), nthreads):
         raise ValueError("orc_matmul_rows: bad arguments")
     return Y, S
+
+
+def f32_to_f16(f: float) -> int:
+    """binary16 bit pattern of float32 f, round to nearest even."""
+    return int(_load().orc_f32_to_f16(float(np.float32(f))))
+
+
+def quantize_q8_0(x: np.ndarray):
+    """Q8_0 activations of float32 x [..., K] (K % 32 == 0): (scales float32
+    [..., K/32], quants int8 [..., K]), per "cera 0.5.2 src/backend/cpu.rs",
+    quantize_f32_to_q8_0_scalar."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    K = x.shape[-1]
+    scales = np.empty(x.shape[:-1] + (K // 32,), dtype=np.float32)
+    quants = np.empty(x.shape, dtype=np.int8)
+    if _load().orc_quantize_q8_0(_ptr(x), x.size, _ptr(scales), _ptr(quants)):
+        raise ValueError("orc_quantize_q8_0: bad arguments")
+    return scales, quants
+
+
+def dequant_q8_0_act(scales: np.ndarray, quants: np.ndarray) -> np.ndarray:
+    """The activation values the Q8_0 codes stand for, scales[b] * quants[e]
+    (exact in float32: an 11-bit scale times an 8-bit code)."""
+    K = quants.shape[-1]
+    s = np.repeat(scales.astype(np.float64), 32, axis=-1).reshape(quants.shape)
+    return (s * quants.astype(np.float64)).astype(np.float32)
+
+
+def matmul_q8act(wtype: int, w: np.ndarray, M: int, K: int, x: np.ndarray, rows=None, nthreads: int = 0):
+    """(Y, S) of the Q8_0-activation product: X is first quantized to Q8_0
+    blocks, then Y[n, m] = sum_k w(m, k) * xq(n, k) with xq the dequantized
+    activations (the pages' int8 decode and prefill arithmetic)."""
+    scales, quants = quantize_q8_0(np.asarray(x, dtype=np.float32).reshape(-1, K))
+    return matmul(wtype, w, M, K, dequant_q8_0_act(scales, quants), rows=rows, nthreads=nthreads)
 
 
 def within(y: np.ndarray, Y: np.ndarray, S: np.ndarray, rel: float, abs_: float):

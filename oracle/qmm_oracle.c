@@ -264,3 +264,52 @@ int orc_matmul_rows(int wtype, const uint8_t *w, int64_t M, int64_t K,
     free(xd);
     return err;
 }
+
+/* ------------------------------------------------------------------------
+ * Activation quantization (Q8_0 activations).
+ * ------------------------------------------------------------------------ */
+
+uint16_t orc_f32_to_f16(float f) {
+    uint32_t bits;
+    memcpy(&bits, &f, 4);
+    const uint16_t sign = (uint16_t)((bits >> 16) & 0x8000u);
+    if (isnan(f)) return (uint16_t)(sign | 0x7e00u);
+    const double v = fabs((double)f);
+    if (v >= 65520.0) return (uint16_t)(sign | 0x7c00u);   /* halfway above 65504 rounds up: infinity */
+    if (v == 0.0) return sign;
+    int ex;
+    (void)frexp(v, &ex);                                   /* v = m 2^ex, m in [0.5, 1) */
+    const int e = ex - 1;                                   /* floor(log2 v) */
+    if (e < -14) {                                          /* subnormal: multiples of 2^-24 */
+        const double r = nearbyint(ldexp(v, 24));           /* ties to even (default rounding) */
+        return (uint16_t)(sign | (uint16_t)r);              /* r == 1024 is the smallest normal */
+    }
+    double r = nearbyint(ldexp(v, 10 - e));                 /* 11 significant bits: [1024, 2048] */
+    int eb = e + 15;
+    if (r == 2048.0) {
+        r = 1024.0;
+        eb += 1;
+    }
+    if (eb >= 31) return (uint16_t)(sign | 0x7c00u);
+    return (uint16_t)(sign | (uint16_t)(eb << 10) | (uint16_t)(r - 1024.0));
+}
+
+int orc_quantize_q8_0(const float *x, int64_t n, float *scales, int8_t *quants) {
+    if (n < 0 || n % 32 || (n && (!x || !scales || !quants))) return -1;
+    for (int64_t b = 0; b < n / 32; ++b) {
+        const float *blk = x + 32 * b;
+        float amax = 0.0f;
+        for (int e = 0; e < 32; ++e) amax = fmaxf(amax, fabsf(blk[e]));
+        const float d = amax / 127.0f;
+        const float r = 1.0f / d;
+        const float id = (d != 0.0f && isfinite(r)) ? r : 0.0f;
+        scales[b] = (float)orc_f16_to_f64(orc_f32_to_f16(d));
+        for (int e = 0; e < 32; ++e) {
+            float q = rintf(blk[e] * id);
+            if (isnan(q)) q = 0.0f;
+            q = q < -128.0f ? -128.0f : (q > 127.0f ? 127.0f : q);
+            quants[32 * b + e] = (int8_t)q;
+        }
+    }
+    return 0;
+}

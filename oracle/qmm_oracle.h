@@ -17,6 +17,9 @@
  *     field order d, dmin, scales, qs; sub-block nibble order; the products
  *     d*sc and dmin*m), gemm_preq_dispatch (k must be a multiple of the block
  *     size; weight bytes >= m * blocks * block_bytes).
+ *   - "cera 0.5.2 src/backend/cpu.rs": quantize_f32_to_q8_0_scalar (the
+ *     Q8_0 activation quantizer of the int8 decode and prefill paths: scale
+ *     amax/127 through binary16, codes rounded half to even and clamped).
  *   - "cera 0.3.1 src/model/gpu_lfm2.rs": GpuLfm2Model::new weight upload
  *     (block byte sizes: Q4_K 144 B, Q6_K 210 B per 256 weights).
  * Readings where the pages are silent (Q8_0 field order, Q4_K 6-bit scale
@@ -70,6 +73,24 @@ int orc_matmul_rows(int wtype, const uint8_t *w, int64_t M, int64_t K,
                     const void *x, int xtype, int64_t N,
                     const int64_t *rows, int64_t nrows,
                     double *Y, double *S, int nthreads);
+
+/*
+ * IEEE binary32 -> binary16 bit pattern, round to nearest even: subnormal
+ * results, overflow to infinity (|f| >= 65520), NaN stays a (quiet) NaN.
+ */
+uint16_t orc_f32_to_f16(float f);
+
+/*
+ * Q8_0 quantization of activations ("cera 0.5.2 src/backend/cpu.rs",
+ * quantize_f32_to_q8_0_scalar), per 32-element block of x[0..n):
+ *   amax = max |x| (NaN elements ignored, as the float max fold does);
+ *   d = amax / 127 (float);  id = 1/d if d != 0 and 1/d is finite, else 0;
+ *   scales[b] = d rounded to binary16 and back;
+ *   quants[e] = rint(x[e] * id) (ties to even), clamped to [-128, 127],
+ *   NaN -> 0 (the saturating float-to-int8 conversion).
+ * All arithmetic in float.  n % 32 != 0 -> -1, else 0.
+ */
+int orc_quantize_q8_0(const float *x, int64_t n, float *scales, int8_t *quants);
 
 #ifdef __cplusplus
 }

@@ -37,6 +37,15 @@ MUTANTS = {
     "matmul_x_index": ("wrow[k] * xr[k]", "wrow[k] * xr[jb->K - 1 - k]"),
     "matmul_abs_sum": ("s += fabs(p)", "s += p"),
     "row_stride": ("w + m * nb * B", "w + m * nb * (B - 1)"),
+    "q8act_ties": ("rintf(blk[e] * id)", "roundf(blk[e] * id)"),
+    "q8act_divisor": ("amax / 127.0f", "amax / 128.0f"),
+    "q8act_scale_f16": ("scales[b] = (float)orc_f16_to_f64(orc_f32_to_f16(d));", "scales[b] = d;"),
+    "q8act_nan_code": ("if (isnan(q)) q = 0.0f;", "if (isnan(q)) q = 1.0f;"),
+    "q8act_id_guard": ("(d != 0.0f && isfinite(r)) ? r : 0.0f", "(d != 0.0f) ? r : 0.0f"),
+    "q8act_clamp": ("q > 127.0f ? 127.0f : q", "q > 126.0f ? 126.0f : q"),
+    "f16_round_even": ("nearbyint(ldexp(v, 10 - e))", "floor(ldexp(v, 10 - e))"),
+    "f16_sign": ("(bits >> 16) & 0x8000u", "(bits >> 17) & 0x8000u"),
+    "f16_subnormal_round": ("nearbyint(ldexp(v, 24))", "floor(ldexp(v, 24))"),
 }
 
 
@@ -57,6 +66,9 @@ def _build_mutant(tmp, name, old, new):
     lib.orc_dequant.argtypes = [ctypes.c_int, p, i64, i64, p]
     lib.orc_matmul_rows.argtypes = [ctypes.c_int, p, i64, i64, p, ctypes.c_int, i64, p, i64, p, p,
                                     ctypes.c_int]
+    lib.orc_f32_to_f16.argtypes = [ctypes.c_float]
+    lib.orc_f32_to_f16.restype = ctypes.c_uint16
+    lib.orc_quantize_q8_0.argtypes = [p, i64, p, p]
     return lib
 
 
@@ -98,6 +110,18 @@ def _pins_fail(lib) -> list[str]:
         St = (np.abs(Wd)[None] * np.abs(x.astype(np.float64))[:, None]).sum(-1)
         if not (np.all(np.abs(Y - Yt) <= 1e-12 * St) and np.allclose(S, St, rtol=1e-12)):
             failed.append(f"textbook:{fmt}")
+    # activation quantizer: worked blocks and binary16 rounding against numpy
+    for case in pins.Q8ACT_CASES:
+        x, scale, q = pins.q8act_case_arrays(case)
+        sc = np.empty(1, dtype=np.float32)
+        qc = np.empty(32, dtype=np.int8)
+        lib.orc_quantize_q8_0(x.ctypes.data, 32, sc.ctypes.data, qc.ctypes.data)
+        if not ((sc[0] == scale or (np.isinf(scale) and np.isinf(sc[0]))) and np.array_equal(qc, q)):
+            failed.append("q8act:" + case[0])
+    v = pins.f16_cases()
+    got = np.array([lib.orc_f32_to_f16(float(a)) for a in v], dtype=np.uint16)
+    if not np.array_equal(got, pins.f16_reference_bits(v)):
+        failed.append("f32_to_f16")
     return failed
 
 

@@ -399,3 +399,127 @@ def test_tolerance_helper():
     assert ok
     ok, _ = oracle.within(np.array([[1.0002, -2.0]]), Y, S, 1e-5, 1e-6)
     assert not ok
+
+
+# ---------------------------------------------------------------------------
+# Q8_0 activation quantizer ("cera 0.5.2 src/backend/cpu.rs",
+# quantize_f32_to_q8_0_scalar): scale amax/127 in float, rounded through
+# binary16; codes rint(x * (1/d)) with ties to even, clamped, NaN -> 0.
+# Worked blocks with closed-form results: (name, {index: x}, scale, {index: code}).
+# ---------------------------------------------------------------------------
+_D127 = float(np.float32(1.0) / np.float32(127.0))
+Q8ACT_CASES = [
+    # amax 127 -> d = 1 exactly, id = 1: codes are x rounded half to even
+    ("unit_scale_ties", {0: 127.0, 1: 2.5, 2: 3.5, 3: -2.5, 4: -127.0, 5: 0.5, 6: 1.5, 7: -0.5},
+     1.0, {0: 127, 1: 2, 2: 4, 3: -2, 4: -127, 5: 0, 6: 2, 7: 0}),
+    # amax 1 -> d = fl(1/127); 1/d rounds to 127 exactly; x = 0.5 is a tie (63.5 -> 64);
+    # the binary16 scale is 2^-7 (1 + 8/1024)
+    ("unit_amax", {0: 1.0, 1: 0.5, 2: -0.25, 3: 0.75}, 2.0 ** -7 * (1 + 8 / 1024),
+     {0: 127, 1: 64, 2: -32, 3: 95}),
+    ("zero_block", {}, 0.0, {}),
+    # a NaN element is skipped by the max fold and gets code 0
+    ("nan_element", {0: 127.0, 1: float("nan"), 2: 5.0}, 1.0, {0: 127, 1: 0, 2: 5}),
+    # amax = inf: d = inf, 1/d = 0 is finite, so id = 0 and every code is 0;
+    # the scale stays infinite
+    ("inf_element", {0: float("inf"), 1: 3.0}, float("inf"), {0: 0, 1: 0}),
+    # subnormal amax: 1/d overflows, id = 0; d underflows binary16 to 0
+    ("subnormal_amax", {0: 1e-40, 1: -5e-41}, 0.0, {0: 0, 1: 0}),
+    # d = 70000 overflows binary16 (scale inf) but the codes use the float d
+    ("f16_overflow_scale", {0: 127.0 * 70000.0, 1: 70000.0, 2: -35000.0}, float("inf"),
+     {0: 127, 1: 1, 2: 0}),
+]
+
+
+def q8act_case_arrays(case):
+    name, xs, scale, codes = case
+    x = np.zeros(32, dtype=np.float32)
+    for i, v in xs.items():
+        x[i] = v
+    q = np.zeros(32, dtype=np.int8)
+    for i, v in codes.items():
+        q[i] = v
+    return x, np.float32(scale), q
+
+
+@pytest.mark.parametrize("case", Q8ACT_CASES, ids=[c[0] for c in Q8ACT_CASES])
+def test_q8_0_act_worked_blocks(case):
+    x, scale, q = q8act_case_arrays(case)
+    s, c = oracle.quantize_q8_0(x)
+    assert s.shape == (1,) and c.shape == (32,)
+    assert s[0] == scale or (np.isinf(scale) and np.isinf(s[0])), (s[0], scale)
+    assert np.array_equal(c, q), c
+
+
+def test_q8_0_act_unit_amax_reciprocal_is_exact():
+    # the reading of the worked block above: fl(1 / fl(1/127)) == 127
+    assert np.float32(1.0) / np.float32(_D127) == np.float32(127.0)
+
+
+def f16_reference_bits(v: np.ndarray) -> np.ndarray:
+    """numpy's float32 -> float16 cast (round to nearest even) as bit patterns."""
+    with np.errstate(over="ignore"):
+        return v.astype(np.float16).view(np.uint16)
+
+
+def f16_cases() -> np.ndarray:
+    rng = np.random.default_rng(20261202)
+    parts = [
+        rng.standard_normal(3000).astype(np.float32) * np.float32(10.0) ** rng.integers(-9, 6, 3000),
+        np.float32(2.0) ** np.arange(-30, 17, dtype=np.float32),
+        # exact ties of binary16 rounding: odd multiples of half a unit in the last place
+        ((np.arange(1, 400, 2, dtype=np.float64) / 2 + 1024) * 2.0 ** -10).astype(np.float32),
+        ((np.arange(1, 200, 2, dtype=np.float64) / 2) * 2.0 ** -24).astype(np.float32),   # subnormal ties
+        np.array([65504, 65519, 65519.998, 65520, 65536, 1e9, 6.1e-5, 6.097555e-05, 5.96e-8, 2.98e-8,
+                  2.9802322e-08, 2.99e-8, 0.0, -0.0, np.inf, -np.inf], dtype=np.float32),
+    ]
+    v = np.concatenate(parts).astype(np.float32)
+    return np.concatenate([v, -v])
+
+
+def test_f32_to_f16_matches_numpy():
+    v = f16_cases()
+    got = np.array([oracle.f32_to_f16(float(a)) for a in v], dtype=np.uint16)
+    assert np.array_equal(got, f16_reference_bits(v))
+    assert (oracle.f32_to_f16(float("nan")) & 0x7c00) == 0x7c00 and (oracle.f32_to_f16(float("nan")) & 0x3ff)
+
+
+def q8act_numpy(x: np.ndarray):
+    """Independent float32 restatement with numpy's own binary16 cast."""
+    b = x.astype(np.float32).reshape(-1, 32)
+    amax = np.fmax.reduce(np.abs(b), axis=1, initial=np.float32(0))
+    with np.errstate(divide="ignore", over="ignore", invalid="ignore"):
+        d = (amax / np.float32(127)).astype(np.float32)
+        r = (np.float32(1) / d).astype(np.float32)
+        idv = np.where((d != 0) & np.isfinite(r), r, np.float32(0)).astype(np.float32)
+        q = np.rint((b * idv[:, None]).astype(np.float32))
+        q = np.where(np.isnan(q), 0, np.clip(q, -128, 127)).astype(np.int8)
+        s = d.astype(np.float16).astype(np.float32)
+    return s, q.reshape(x.shape)
+
+
+def test_q8_0_act_random_blocks_match_numpy():
+    x = synth.gen_x(8, 1024, "q8act-pin")
+    x[0, :32] *= np.float32(1e-3)
+    x[1, 32:64] *= np.float32(3e4)
+    s, q = oracle.quantize_q8_0(x)
+    s2, q2 = q8act_numpy(x.reshape(-1))
+    assert np.array_equal(s.reshape(-1), s2) and np.array_equal(q.reshape(-1), q2.reshape(-1))
+
+
+def test_q8act_matmul_one_hot_closed_form():
+    # X = c * e_k: the block of k has amax c, so its code at k is 127 and
+    # y[m] = w(m, k) * 127 * f16(c / 127)
+    fmt, M, K, k, c = synth.Q4_0, 8, 256, 77, np.float32(3.0)
+    w = synth.gen_weights(fmt, M, K, "q8act-onehot")
+    x = np.zeros((1, K), dtype=np.float32)
+    x[0, k] = c
+    Y, S = oracle.matmul_q8act(fmt, w, M, K, x)
+    scale = np.float64(np.float32(c / np.float32(127)).astype(np.float16))
+    Wd = oracle.dequant(fmt, w, M, K)
+    assert np.array_equal(Y[0], Wd[:, k] * 127 * scale)
+    assert np.array_equal(S[0], np.abs(Y[0]))
+
+
+def test_q8act_bad_length_rejected():
+    with pytest.raises(ValueError):
+        oracle.quantize_q8_0(np.zeros(31, dtype=np.float32))
