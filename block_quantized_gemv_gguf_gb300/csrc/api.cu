@@ -24,6 +24,19 @@ std::atomic<uint64_t> g_wait_limit{1ull << 31};   // ~1 s at 2 GHz
 // Static-weights mode (programmatic dependent launch): -1 = not set through
 // the API, take QMM_STATIC_WEIGHTS from the environment.
 std::atomic<int> g_static_weights{-1};
+// Integer tensor-core GEMV for N <= 2 (exact int8 digits of X): -1 = not set
+// through the API, take QMM_GEMV_I8 from the environment (default off: on
+// this part it measures no faster than the bf16 kernel).
+std::atomic<int> g_gemv_i8{-1};
+bool gemv_i8_on() {
+    const int v = g_gemv_i8.load();
+    if (v >= 0) return v != 0;
+    static const bool env = [] {
+        const char *e = std::getenv("QMM_GEMV_I8");
+        return e && *e && std::atoi(e) != 0;
+    }();
+    return env;
+}
 // Set while qmm_matmul_host runs its compute call: that call follows a
 // host-to-device copy, not a kernel, so it is launched the ordinary way.
 thread_local bool t_after_copy = false;
@@ -138,17 +151,19 @@ const Settings &settings() {
 // Common validation of W, M, K, X, N, Y.
 // ybytes_override: the size of the output actually written at Y (argmax
 // mode writes N entries, not N x M); 0 means N * M * 4.
+// xt == X_CODES: X holds int8 codes (N * K bytes, any alignment).
+constexpr int X_CODES = 100;
 qmm_status validate(int wt, const void *W, size_t w_bytes, int64_t M, int64_t K, const void *X, int xt,
                     int64_t N, const float *Y, int64_t max_n, int &E, int &B, size_t ybytes_override = 0) {
     if (!block_geom(wt, E, B)) return QMM_ERR_INVALID_ARG;
-    if (xt != QMM_X_F32 && xt != QMM_X_BF16) return QMM_ERR_INVALID_ARG;
+    if (xt != QMM_X_F32 && xt != QMM_X_BF16 && xt != X_CODES) return QMM_ERR_INVALID_ARG;
     if (!W || !X || !Y) return QMM_ERR_INVALID_ARG;
     if (M < 1 || K < 1 || M > (1ll << 30) || K > (1ll << 24)) return QMM_ERR_INVALID_ARG;
     if (N < 1 || N > max_n) return QMM_ERR_INVALID_ARG;
     if (K % E) return QMM_ERR_INVALID_ARG;
     const size_t need = (size_t)M * (size_t)(K / E) * (size_t)B;
     if (w_bytes < need) return QMM_ERR_INVALID_ARG;
-    const size_t xs = xt == QMM_X_F32 ? 4 : 2;
+    const size_t xs = xt == QMM_X_F32 ? 4 : (xt == QMM_X_BF16 ? 2 : 1);
     if (((uintptr_t)X) % xs || ((uintptr_t)Y) % 4) return QMM_ERR_INVALID_ARG;
     const size_t ybytes = ybytes_override ? ybytes_override : (size_t)N * (size_t)M * 4;
     if (overlaps(Y, ybytes, W, need) || overlaps(Y, ybytes, X, (size_t)N * (size_t)K * xs))
@@ -192,17 +207,43 @@ struct SegIn {
     float *Y;
 };
 
+// Plan of the integer GEMV (mode 0: exact digits, 1: Q8_0 activations), or
+// false when no variant holds the K slice.
+bool plan_i8(int mode, int wt, int64_t m_total, int64_t K, int N, int xbf16, int num_sms, GemvPlan &p) {
+    const Settings &cfg = settings();
+    const int rows = cfg.gemv_rows ? (cfg.gemv_rows >= 128 ? 128 : 64) : gemv_tile_rows(m_total, num_sms);
+    const int rg = mode == 0 && rows == 128 && cfg.gemv_rg == 2 ? 2 : 1;
+    const int maxc = mode == 0 ? gemv_i8_exact_maxc(wt, N, xbf16, rows, rg) : gemv_i8_q8_maxc(wt, N, rows);
+    if (maxc <= 0) return false;
+    const int ks = plan_ks_host((m_total + rows - 1) / rows, (int)(K / 256), num_sms, maxc, cfg.gemv_ks);
+    if (ks <= 0) return false;
+    p.resident = 2;
+    p.rows = rows;
+    p.rg = rg;
+    p.ks = ks;
+    return true;
+}
+
+// xscales != nullptr: Q8_0-activation mode, X = quants int8 [N][K] and
+// xscales f32 [N][K/32] (the fast path only, else QMM_ERR_UNSUPPORTED).
 qmm_status gemv_segments(int wt, const SegIn *seg, int nseg, int64_t K, const void *X, int xt, int64_t N,
                          void *stream, unsigned long long *amax = nullptr, int32_t *idx = nullptr,
-                         float *val = nullptr) {
+                         float *val = nullptr, const float *xscales = nullptr) {
     if (nseg < 1 || nseg > QMM_MAX_SEGS || (amax && nseg != 1)) return QMM_ERR_INVALID_ARG;
+    const bool q8 = xscales != nullptr;
+    if (q8 && (N < 1 || N > QMM_GEMV_MAX_N)) return QMM_ERR_INVALID_ARG;
     int E = 0, B = 0;
     int64_t m_total = 0;
     for (int i = 0; i < nseg; ++i) {
-        const qmm_status s = validate(wt, seg[i].W, seg[i].w_bytes, seg[i].M, K, X, xt, N,
-                                      amax ? reinterpret_cast<const float *>(amax) : seg[i].Y, QMM_GEMV_MAX_N, E, B,
-                                      amax ? (size_t)(N + 1) * 8 : 0);
+        const qmm_status s =
+            validate(wt, seg[i].W, seg[i].w_bytes, seg[i].M, K, X, q8 ? X_CODES : xt, N,
+                     amax ? reinterpret_cast<const float *>(amax) : seg[i].Y, QMM_GEMV_MAX_N, E, B,
+                     amax ? (size_t)(N + 1) * 8 : (size_t)N * (size_t)seg[i].M * 4);
         if (s != QMM_OK) return s;
+        if (q8 && (overlaps(amax ? static_cast<const void *>(amax) : seg[i].Y,
+                            amax ? (size_t)(N + 1) * 8 : (size_t)N * (size_t)seg[i].M * 4, xscales,
+                            (size_t)N * (size_t)(K / 32) * 4)))
+            return QMM_ERR_INVALID_ARG;
         m_total += seg[i].M;
         for (int j = 0; j < nseg && !amax; ++j) {   // no output may overlap another matrix or output
             const size_t yi = (size_t)N * (size_t)seg[i].M * 4;
@@ -220,12 +261,21 @@ qmm_status gemv_segments(int wt, const SegIn *seg, int nseg, int64_t K, const vo
     // byte-addressed kernel, which computes the same sums.
     bool fast = K % 256 == 0 && row_bytes % 16 == 0 && (uintptr_t)X % 16 == 0 && m_total <= (1ll << 31) - 1;
     for (int i = 0; i < nseg; ++i) fast = fast && (uintptr_t)seg[i].W % 16 == 0;
+    if (q8) fast = fast && (uintptr_t)xscales % 16 == 0;
     if (fast) {
         EncodeTiledFn enc = encode_fn();
         if (!enc) return QMM_ERR_CUDA;
         const Settings &cfg = settings();
         const GemvTuning tun{cfg.gemv_rows, cfg.gemv_rg, cfg.gemv_ks, cfg.gemv_res};
-        const GemvPlan plan = plan_gemv(m_total, K, (int)N, xt == QMM_X_BF16, di.num_sms, tun);
+        GemvPlan plan{};
+        bool i8 = false;
+        if (q8) {
+            if (!plan_i8(1, wt, m_total, K, (int)N, 0, di.num_sms, plan)) return QMM_ERR_UNSUPPORTED;
+            i8 = true;
+        } else if (gemv_i8_on() && N <= 2) {
+            i8 = plan_i8(0, wt, m_total, K, (int)N, xt == QMM_X_BF16, di.num_sms, plan);
+        }
+        if (!i8) plan = plan_gemv(m_total, K, (int)N, xt == QMM_X_BF16, di.num_sms, tun);
         GemvSegs segs{};
         segs.nseg = nseg;
         const int win = gemv_window_bytes(wt);
@@ -241,6 +291,13 @@ qmm_status gemv_segments(int wt, const SegIn *seg, int nseg, int64_t K, const vo
             segs.Y[i] = seg[i].Y;
             segs.M[i] = (int)seg[i].M;
         }
+        const bool pdl = amax ? false : static_weights();
+        if (q8)
+            return from_cuda(launch_gemv_i8_q8(wt, plan, segs, static_cast<const int8_t *>(X), xscales, K, (int)N, pdl,
+                                               di.status, g_wait_limit.load(), st, amax, idx, val));
+        if (i8)
+            return from_cuda(launch_gemv_i8_exact(wt, plan, segs, X, xt == QMM_X_BF16, K, (int)N, pdl, di.status,
+                                                  g_wait_limit.load(), st, amax, idx, val));
         CUtensorMap xmap;
         const int xes = xt == QMM_X_F32 ? 4 : 2;
         cuuint64_t xdims[2] = {(cuuint64_t)K, (cuuint64_t)N};
@@ -256,7 +313,7 @@ qmm_status gemv_segments(int wt, const SegIn *seg, int nseg, int64_t K, const vo
                                          amax ? false : static_weights(), di.status, g_wait_limit.load(), st, amax,
                                          idx, val));
     }
-    if (amax) return QMM_ERR_UNSUPPORTED;
+    if (amax || q8) return QMM_ERR_UNSUPPORTED;
     for (int i = 0; i < nseg; ++i) {
         const qmm_status s = from_cuda(launch_gemv_generic(wt, static_cast<const uint8_t *>(seg[i].W), seg[i].M, K, X,
                                                            xt == QMM_X_BF16, (int)N, seg[i].Y, st));
@@ -460,6 +517,53 @@ qmm_status qmm_last_device_error(void *stream) {
 }
 
 void qmm_set_static_weights(int on) { g_static_weights.store(on ? 1 : 0); }
+
+void qmm_set_gemv_i8(int on) { g_gemv_i8.store(on < 0 ? -1 : (on ? 1 : 0)); }
+
+size_t qmm_q8act_workspace_bytes(int64_t N, int64_t K) {
+    if (N < 1 || K < 1) return 0;
+    return ((size_t)N * (size_t)K + 15) / 16 * 16 + (size_t)N * (size_t)(K / 32) * 4;
+}
+
+qmm_status qmm_quantize_q8_0(const void *X, qmm_xtype xt, int64_t N, int64_t K, float *scales, int8_t *quants,
+                             void *stream) {
+    if (!X || !scales || !quants || (xt != QMM_X_F32 && xt != QMM_X_BF16)) return QMM_ERR_INVALID_ARG;
+    if (N < 1 || K < 32 || K % 32 || N > (1ll << 30) || K > (1ll << 24)) return QMM_ERR_INVALID_ARG;
+    const size_t xs = xt == QMM_X_F32 ? 4 : 2;
+    if ((uintptr_t)X % xs || (uintptr_t)scales % 4) return QMM_ERR_INVALID_ARG;
+    const size_t nx = (size_t)N * (size_t)K;
+    if (overlaps(scales, nx / 32 * 4, X, nx * xs) || overlaps(quants, nx, X, nx * xs) ||
+        overlaps(quants, nx, scales, nx / 32 * 4))
+        return QMM_ERR_INVALID_ARG;
+    return from_cuda(launch_quantize_q8_0(X, xt == QMM_X_BF16, (int64_t)nx, scales, quants, static_weights(),
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+qmm_status qmm_gemv_preq(qmm_wtype wt, const void *W, size_t w_bytes, int64_t M, int64_t K, const float *scales,
+                         const int8_t *quants, int64_t N, float *Y, void *stream) {
+    if (!scales || !quants) return QMM_ERR_INVALID_ARG;
+    const SegIn seg{W, w_bytes, M, Y};
+    return gemv_segments(wt, &seg, 1, K, quants, QMM_X_F32, N, stream, nullptr, nullptr, nullptr, scales);
+}
+
+qmm_status qmm_gemv_q8act(qmm_wtype wt, const void *W, size_t w_bytes, int64_t M, int64_t K, const void *X,
+                          qmm_xtype xt, int64_t N, float *Y, void *workspace, size_t ws_bytes, void *stream) {
+    int E, B;
+    qmm_status s = validate(wt, W, w_bytes, M, K, X, xt, N, Y, QMM_GEMV_MAX_N, E, B);
+    if (s != QMM_OK) return s;
+    const size_t need = qmm_q8act_workspace_bytes(N, K);
+    if (!workspace || ws_bytes < need || (uintptr_t)workspace % 16) return QMM_ERR_INVALID_ARG;
+    const size_t xs = xt == QMM_X_F32 ? 4 : 2;
+    if (overlaps(workspace, need, Y, (size_t)N * M * 4) || overlaps(workspace, need, X, (size_t)N * K * xs) ||
+        overlaps(workspace, need, W, (size_t)M * (K / E) * B))
+        return QMM_ERR_INVALID_ARG;
+    if (K % 256) return QMM_ERR_UNSUPPORTED;
+    int8_t *q = static_cast<int8_t *>(workspace);
+    float *sc = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + ((size_t)N * K + 15) / 16 * 16);
+    s = qmm_quantize_q8_0(X, xt, N, K, sc, q, stream);
+    if (s != QMM_OK) return s;
+    return qmm_gemv_preq(wt, W, w_bytes, M, K, sc, q, N, Y, stream);
+}
 
 void qmm_set_wait_limit(uint64_t cycles) {
     if (cycles < 1) cycles = 1;

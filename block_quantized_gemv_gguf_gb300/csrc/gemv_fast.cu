@@ -59,6 +59,9 @@ template <int F, int NT, int CW> struct GL {
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int TOTAL = OFF_MISC + 16;
     static constexpr int SMEM = TOTAL + 1024;
+    // CTAs per SM the shared memory allows (at most 4): the register budget
+    // the compiler may use without lowering that occupancy
+    static constexpr int MINB = 232448 / SMEM >= 4 ? 4 : (232448 / SMEM >= 1 ? 232448 / SMEM : 1);
     static_assert(XR * XSLOT >= ROWS * 16 * 4, "reduction buffer fits in the X ring");
     static_assert(XSLOT % 16 == 0 && STAGE % 1024 == 0 && XRAW % 1024 == 0, "alignment");
     static_assert(SMEM <= 232448, "shared memory");
@@ -390,7 +393,7 @@ __device__ __forceinline__ void compute_chunk(float (&acc)[NT][4], const uint8_t
 }
 
 template <int F, int NT, int P, bool XBF16, int CW>
-__global__ void __launch_bounds__(GL<F, NT, CW>::THREADS)
+__global__ void __launch_bounds__(GL<F, NT, CW>::THREADS, GL<F, NT, CW>::MINB)
     gemv_mma_kernel(const __grid_constant__ GemvSegs segs, const __grid_constant__ CUtensorMap xmap, int K, int N,
                     int cps, unsigned *status, uint64_t wait_limit, AmaxOut amax) {
     using L = GL<F, NT, CW>;
@@ -579,13 +582,14 @@ template <int F, int NC, int CW, int RG> struct GR {
     static constexpr int OFF_BAR = OFF_SCT + SCT;
     static constexpr int OFF_MISC = OFF_BAR + (2 * S + 1) * 8;
     static constexpr int SMEM = OFF_MISC + 16 + 1024;
+    static constexpr int MINB = 232448 / SMEM >= 4 ? 4 : (232448 / SMEM >= 1 ? 232448 / SMEM : 1);
     static_assert(ROWS * 16 * 4 <= XRES, "reduction buffer fits in the fragment area");
     static_assert(STAGE % 1024 == 0 && OFF_BAR % 8 == 0, "alignment");
     static_assert(SMEM <= 232448, "shared memory");
 };
 
 template <int F, int NC, int P, bool XBF16, int CW, int RG>
-__global__ void __launch_bounds__(GR<F, NC, CW, RG>::THREADS)
+__global__ void __launch_bounds__(GR<F, NC, CW, RG>::THREADS, GR<F, NC, CW, RG>::MINB)
     gemv_res_kernel(const __grid_constant__ GemvSegs segs, const void *__restrict__ Xv, int K, int N, int cps,
                     unsigned *status, uint64_t wait_limit, AmaxOut amax) {
     using L = GR<F, NC, CW, RG>;
@@ -864,6 +868,10 @@ cudaError_t launch_f(const GemvCall &c) {
 }
 
 }  // namespace
+
+int plan_ks_host(int64_t tiles, int nchunks, int num_sms, int max_cps, int force) {
+    return plan_ks(tiles, nchunks, num_sms, max_cps, force);
+}
 
 int gemv_tile_rows(int64_t M, int num_sms) {
     // 128-row tiles (8 compute warps) once there are enough rows to fill the

@@ -41,11 +41,9 @@ __device__ __forceinline__ uint32_t ldw(const uint8_t *p) { return MIS ? ld32_of
 
 // (a0, a1) += (s0, s1) * (d0, d1), one packed f32x2 FMA.
 __device__ __forceinline__ void ffma2(float &a0, float &a1, float s0, float s1, float d0, float d1) {
-    asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
-        "mov.b64 ra, {%2,%3};\n\tmov.b64 rb, {%4,%5};\n\tmov.b64 rc, {%0,%1};\n\t"
-        "fma.rn.f32x2 rc, ra, rb, rc;\n\tmov.b64 {%0,%1}, rc;\n\t}"
-        : "+f"(a0), "+f"(a1)
-        : "f"(s0), "f"(s1), "f"(d0), "f"(d1));
+    const float2 r = __ffma2_rn(make_float2(s0, s1), make_float2(d0, d1), make_float2(a0, a1));
+    a0 = r.x;
+    a1 = r.y;
 }
 
 __device__ __forceinline__ float ld_dsmem_f32(const float *local, uint32_t rank) {

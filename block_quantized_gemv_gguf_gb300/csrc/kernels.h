@@ -22,9 +22,9 @@ struct GemvTuning {
     int resident;   // 0 disables the resident-X kernel
 };
 
-// What will run: the resident-X kernel (P * N <= 2 MMA columns) or the ring
-// kernel, its tile height (= the weight tensor map's box height), row groups
-// per warp and K split.
+// What will run: the resident-X kernel (P * N <= 2 MMA columns; resident ==
+// 1), the ring kernel (0) or the integer kernel (2), its tile height (= the
+// weight tensor map's box height), row groups per warp and K split.
 struct GemvPlan {
     int resident;
     int rows;
@@ -57,6 +57,33 @@ cudaError_t launch_gemv_mma(int fmt, const GemvPlan &plan, const GemvSegs &segs,
                             const void *X, int xbf16, int64_t K, int N, bool pdl, unsigned *status, uint64_t limit,
                             cudaStream_t st, unsigned long long *amax_ws = nullptr, int32_t *idx = nullptr,
                             float *val = nullptr);
+
+// Integer tensor-core GEMV (mma.sync m16n8k32 on the weights' integer codes),
+// same weight maps, segments, plans and argmax mode as launch_gemv_mma.
+//  * exact: X f32 or bf16 [N][K] as exact int8 digits; N <= 2 (Q6_K: N == 1).
+//  * q8:    X given as Q8_0 activations: quants int8 [N][K], scales f32
+//           [N][K/32] (16-byte aligned); N <= 16.
+// *_maxc: the largest K slice (256-weight chunks) one CTA can hold for that
+// variant and tile height (0: unsupported), the bound for the K split.
+int gemv_i8_exact_maxc(int fmt, int N, int xbf16, int rows, int rg);
+int gemv_i8_q8_maxc(int fmt, int N, int rows);
+cudaError_t launch_gemv_i8_exact(int fmt, const GemvPlan &plan, const GemvSegs &segs, const void *X, int xbf16,
+                                 int64_t K, int N, bool pdl, unsigned *status, uint64_t limit, cudaStream_t st,
+                                 unsigned long long *amax_ws = nullptr, int32_t *idx = nullptr, float *val = nullptr);
+cudaError_t launch_gemv_i8_q8(int fmt, const GemvPlan &plan, const GemvSegs &segs, const int8_t *quants,
+                              const float *scales, int64_t K, int N, bool pdl, unsigned *status, uint64_t limit,
+                              cudaStream_t st, unsigned long long *amax_ws = nullptr, int32_t *idx = nullptr,
+                              float *val = nullptr);
+
+// Q8_0 activations of X (f32 or bf16, count % 32 == 0): scales[count/32],
+// quants[count].  pdl: programmatic dependent of the preceding kernel.
+cudaError_t launch_quantize_q8_0(const void *X, int xbf16, int64_t count, float *scales, int8_t *quants, bool pdl,
+                                 cudaStream_t st);
+
+// K split of a GEMV over `tiles` row tiles: the smallest power of two (<= 8)
+// giving at least 1.5 CTAs per SM, and (max_cps > 0) slices of at most
+// max_cps chunks; force > 0 requests a split.  0: no split fits max_cps.
+int plan_ks_host(int64_t tiles, int nchunks, int num_sms, int max_cps, int force);
 
 // Raw bytes of one 256-weight chunk of a row in the GEMV's staging.
 int gemv_window_bytes(int fmt);

@@ -27,7 +27,8 @@ GEMV_MAX_N, GEMM_MAX_N = 16, 512
 BLOCK = {Q8_0: (32, 34), Q4_0: (32, 18), Q4_K: (256, 144), Q6_K: (256, 210)}
 EXPORTS = ("qmm_gemv", "qmm_gemv_argmax", "qmm_gemv_multi", "qmm_gemm", "qmm_gemm_workspace_bytes", "qmm_matmul", "qmm_matmul_host",
            "qmm_dequant", "qmm_block_info", "qmm_last_device_error", "qmm_status_str",
-           "qmm_set_wait_limit", "qmm_set_static_weights")
+           "qmm_set_wait_limit", "qmm_set_static_weights", "qmm_set_gemv_i8", "qmm_quantize_q8_0",
+           "qmm_gemv_preq", "qmm_q8act_workspace_bytes", "qmm_gemv_q8act")
 
 _lock = threading.Lock()
 _lib = None
@@ -70,8 +71,15 @@ def load() -> ctypes.CDLL:
         lib.qmm_set_wait_limit.restype = None
         lib.qmm_set_static_weights.argtypes = [ctypes.c_int]
         lib.qmm_set_static_weights.restype = None
+        lib.qmm_set_gemv_i8.argtypes = [ctypes.c_int]
+        lib.qmm_set_gemv_i8.restype = None
+        lib.qmm_quantize_q8_0.argtypes = [p, ci, i64, i64, p, p, p]
+        lib.qmm_gemv_preq.argtypes = [ci, p, sz, i64, i64, p, p, i64, p, p]
+        lib.qmm_q8act_workspace_bytes.argtypes = [i64, i64]
+        lib.qmm_q8act_workspace_bytes.restype = sz
+        lib.qmm_gemv_q8act.argtypes = [ci, p, sz, i64, i64, p, ci, i64, p, p, sz, p]
         for f in ("qmm_gemv", "qmm_gemv_argmax", "qmm_gemv_multi", "qmm_gemm", "qmm_matmul", "qmm_matmul_host", "qmm_dequant", "qmm_block_info",
-                  "qmm_last_device_error"):
+                  "qmm_last_device_error", "qmm_quantize_q8_0", "qmm_gemv_preq", "qmm_gemv_q8act"):
             getattr(lib, f).restype = ci
         _lib = lib
         return lib
@@ -211,6 +219,51 @@ def qmm_set_static_weights(on: bool) -> None:
     """Static-weights mode (see include/qmm.h): weights stream before the
     preceding kernel on the stream ends; W must not be written meanwhile."""
     load().qmm_set_static_weights(1 if on else 0)
+
+
+def qmm_set_gemv_i8(on: int) -> None:
+    """GEMV kernel for N <= 2 (see include/qmm.h): 1 integer kernel, 0 bf16
+    kernel, -1 the environment's choice (QMM_GEMV_I8, default off)."""
+    load().qmm_set_gemv_i8(int(on))
+
+
+def qmm_quantize_q8_0(X, N, K, scales, quants, stream=None, xt=None) -> int:
+    return load().qmm_quantize_q8_0(_ptr(X), _xtype(X) if xt is None else xt, N, K, _ptr(scales), _ptr(quants),
+                                    _stream(stream))
+
+
+def qmm_gemv_preq(wt, W, M, K, scales, quants, N, Y, stream=None, w_bytes=None) -> int:
+    return load().qmm_gemv_preq(wt, _ptr(W), _nbytes(W) if w_bytes is None else w_bytes, M, K, _ptr(scales),
+                                _ptr(quants), N, _ptr(Y), _stream(stream))
+
+
+def qmm_q8act_workspace_bytes(N, K) -> int:
+    return load().qmm_q8act_workspace_bytes(N, K)
+
+
+def qmm_gemv_q8act(wt, W, M, K, X, N, Y, workspace, ws_bytes=None, stream=None, w_bytes=None, xt=None) -> int:
+    return load().qmm_gemv_q8act(wt, _ptr(W), _nbytes(W) if w_bytes is None else w_bytes, M, K, _ptr(X),
+                                 _xtype(X) if xt is None else xt, N, _ptr(Y), _ptr(workspace),
+                                 _nbytes(workspace) if ws_bytes is None else ws_bytes, _stream(stream))
+
+
+def quantize_q8_0(X, stream=None):
+    """(scales f32 [N, K/32], quants int8 [N, K]) of X [N, K] (f32 or bf16)."""
+    N, K = X.shape
+    scales = torch.empty((N, K // 32), dtype=torch.float32, device=X.device)
+    quants = torch.empty((N, K), dtype=torch.int8, device=X.device)
+    _check(qmm_quantize_q8_0(X, N, K, scales, quants, stream), "qmm_quantize_q8_0")
+    return scales, quants
+
+
+def gemv_q8act(wt, W, M, K, X, Y=None, workspace=None, stream=None):
+    """Y [N, M] of the Q8_0-activation GEMV of X [N, K] (1 <= N <= 16)."""
+    N = _shape(X, K)
+    Y = torch.empty((N, M), dtype=torch.float32, device=X.device) if Y is None else Y
+    if workspace is None:
+        workspace = torch.empty(qmm_q8act_workspace_bytes(N, K), dtype=torch.uint8, device=X.device)
+    _check(qmm_gemv_q8act(wt, W, M, K, X, N, Y, workspace, stream=stream), "qmm_gemv_q8act")
+    return Y
 
 
 def _check(s: int, what: str):

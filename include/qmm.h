@@ -270,6 +270,67 @@ QMM_API void qmm_set_static_weights(int on);
  */
 QMM_API void qmm_set_wait_limit(uint64_t cycles);
 
+/*
+ * GEMV kernel choice for 1 <= N <= 2 (Q6_K: N == 1): on (1, or QMM_GEMV_I8=1
+ * in the environment) runs the integer tensor-core kernel, which feeds X to
+ * mma.sync as exact int8 digits (per
+ * 32-element block: T = rint(x 2^(29-E)), E the exponent of the block's
+ * largest |x|, in four base-256 digits; |x - T 2^(E-29)| <= 2^-30 * 2^E),
+ * and the weights' integer codes as 8-bit operands; off (0, the default)
+ * runs the bf16 tensor-core kernel for every N.  Both meet the GEMV
+ * tolerance of qmm_gemv.
+ * -1 returns to the environment's choice.  Process-wide; takes effect at
+ * the next call.  X blocks whose largest |x| is below 2^-98 count as zero
+ * on the integer kernel, and a block holding a NaN or an infinity gives NaN
+ * outputs.
+ */
+QMM_API void qmm_set_gemv_i8(int on);
+
+/*
+ * Q8_0 activations ("cera 0.5.2 src/backend/cpu.rs",
+ * quantize_f32_to_q8_0_into / quantize_f32_to_q8_0_scalar).  For each
+ * 32-element block of X[N][K] (f32, or bf16 widened exactly): amax = max |x|
+ * (NaN elements ignored), d = amax / 127, id = 1/d if d != 0 and 1/d is
+ * finite else 0; scales[b] = d rounded to binary16 and back to f32;
+ * quants[e] = rint(x * id) (ties to even) clamped to [-128, 127], NaN -> 0.
+ * Every step is correctly rounded f32, so the codes and scales equal any
+ * IEEE implementation's bit for bit.  scales: f32 [N][K/32], quants: int8
+ * [N][K], device, caller-owned, not overlapping X or each other.  K % 32 ==
+ * 0.  Asynchronous on `stream`.
+ */
+QMM_API qmm_status qmm_quantize_q8_0(const void *X, qmm_xtype xt, int64_t N, int64_t K, float *scales,
+                                     int8_t *quants, void *stream);
+
+/*
+ * Y[n, m] = sum_b d_w(m, b) scales[n][b] sum_{e in b} q_w(m, e) quants[n][e]
+ * (Q4_0 and Q6_K codes with their offsets, Q4_K with its min term), i.e.
+ * the projection of dequant(W) on the dequantized Q8_0 activations: the
+ * int8 decode arithmetic of "cera 0.5.2 src/backend/cpu.rs"
+ * (gemm_preq_dispatch: weights against pre-quantized activation scales and
+ * quants).  1 <= N <= 16.  The integer sums are exact; only the f32
+ * combination of block scales rounds (|Y - exact| <= 1e-5 * sum|w x_q| +
+ * 1e-6).  Needs the tensor-core geometry: K % 256 == 0, W, scales and
+ * quants 16-byte aligned, 16-byte row pitch; otherwise
+ * QMM_ERR_UNSUPPORTED (there is no byte-addressed variant).  Y: f32 [N][M],
+ * overwritten, not overlapping any input.
+ */
+QMM_API qmm_status qmm_gemv_preq(qmm_wtype wt, const void *W, size_t w_bytes, int64_t M, int64_t K,
+                                 const float *scales, const int8_t *quants, int64_t N, float *Y, void *stream);
+
+/* Workspace of qmm_gemv_q8act: the quants (N*K bytes, padded to 16) then the
+ * scales (N*K/32 floats). */
+QMM_API size_t qmm_q8act_workspace_bytes(int64_t N, int64_t K);
+
+/*
+ * qmm_quantize_q8_0 of X into `workspace` followed by qmm_gemv_preq on it
+ * (two kernels, stream-ordered): the Q8_0-activation GEMV of f32 or bf16 X,
+ * 1 <= N <= 16.  workspace: device, 16-byte aligned, at least
+ * qmm_q8act_workspace_bytes(N, K), not overlapping W, X or Y.
+ */
+QMM_API qmm_status qmm_gemv_q8act(qmm_wtype wt, const void *W, size_t w_bytes, int64_t M, int64_t K,
+                                  const void *X, qmm_xtype xt, int64_t N, float *Y, void *workspace,
+                                  size_t ws_bytes, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

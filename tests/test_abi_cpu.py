@@ -84,3 +84,23 @@ def test_invalid_arguments_rejected_before_any_device_work(lib):
     assert L.qmm_gemm(qmm.Q4_K, 4096, 1 << 20, 16, 256, 1 << 24, 0, 64, 1 << 28, None, 0, None) == \
         qmm.ERR_INVALID_ARG
     assert L.qmm_dequant(qmm.Q6_K, 4096, 210, 1, 256, None, None) == qmm.ERR_INVALID_ARG
+
+
+def test_q8_activation_entry_points_validate_exact_sizes(lib):
+    # Codes are N*K bytes: an output right after them is not an overlap, so
+    # validation passes and the call only fails for want of a device.
+    L = lib
+    wt, M, K, N = qmm.Q4_0, 64, 512, 2
+    base = 1 << 32                                   # fake, never dereferenced
+    W, S, Q = base, base + (1 << 20), base + (2 << 20)
+    Y = Q + N * K                                    # adjacent to the codes
+    assert L.qmm_gemv_preq(wt, W, M * 16 * 18, M, K, S, Q, N, Y, None) == qmm.ERR_CUDA
+    assert L.qmm_gemv_preq(wt, W, M * 16 * 18, M, K, S, Q, N, Q + N * K - 4, None) == qmm.ERR_INVALID_ARG
+    assert L.qmm_gemv_preq(wt, W, M * 16 * 18, M, K, S, Q, 17, Y, None) == qmm.ERR_INVALID_ARG
+    assert L.qmm_gemv_preq(wt, W, M * 16 * 18, M, K, None, Q, N, Y, None) == qmm.ERR_INVALID_ARG
+    assert L.qmm_quantize_q8_0(base, qmm.X_F32, N, 500, S, Q, None) == qmm.ERR_INVALID_ARG     # K % 32
+    assert L.qmm_quantize_q8_0(base, qmm.X_F32, N, K, base + 64, Q, None) == qmm.ERR_INVALID_ARG  # scales on X
+    assert L.qmm_q8act_workspace_bytes(N, K) == N * K + N * (K // 32) * 4
+    ws = base + (3 << 20)
+    assert L.qmm_gemv_q8act(wt, W, M * 16 * 18, M, K, base + (4 << 20), qmm.X_F32, N, base + (5 << 20), ws, 16,
+                            None) == qmm.ERR_INVALID_ARG                                         # small workspace
