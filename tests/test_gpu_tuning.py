@@ -54,6 +54,9 @@ COMBOS = [
     {"QMM_GEMV_ROWS": "256", "QMM_GEMV_KS": "1", "QMM_GEMV_RESIDENT": "1"},
     {"QMM_GEMV_ROWS": "128", "QMM_GEMV_KS": "1", "QMM_GEMV_RESIDENT": "0"},
     {"QMM_GEMV_ROWS": "64", "QMM_GEMV_KS": "4", "QMM_GEMV_RESIDENT": "0"},
+    # the integer kernel (exact int8 digits) for N <= 2
+    {"QMM_GEMV_ROWS": "64", "QMM_GEMV_KS": "2", "QMM_GEMV_I8": "1"},
+    {"QMM_GEMV_ROWS": "128", "QMM_GEMV_RG": "2", "QMM_GEMV_KS": "1", "QMM_GEMV_I8": "1"},
 ]
 
 
