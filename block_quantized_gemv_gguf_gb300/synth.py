@@ -11,6 +11,7 @@ Distributions (the workloads of the projection-matmul benchmarks):
          128 uniform nibble bytes
   Q6_K : 128 uniform ql bytes, 64 uniform qh bytes, 16 int8 scales
          ~ U{-64..63}, d ~ U[1e-4, 1e-3] as f16
+  Q5_K : as Q4_K, with 32 uniform qh bytes between the scales and qs
   X    : N(0, 1) drawn in double and rounded to f32; bf16 X is the
          round-to-nearest-even bf16 of those same f32 values.
 Block byte layouts (field offsets) are the ones documented in include/qmm.h.
@@ -26,9 +27,9 @@ import numpy as np
 
 BASE_SEED = 20261202
 
-Q8_0, Q4_0, Q4_K, Q6_K = 0, 1, 2, 3
-NAMES = {Q8_0: "Q8_0", Q4_0: "Q4_0", Q4_K: "Q4_K", Q6_K: "Q6_K"}
-BLOCK = {Q8_0: (32, 34), Q4_0: (32, 18), Q4_K: (256, 144), Q6_K: (256, 210)}
+Q8_0, Q4_0, Q4_K, Q6_K, Q5_K = 0, 1, 2, 3, 4
+NAMES = {Q8_0: "Q8_0", Q4_0: "Q4_0", Q4_K: "Q4_K", Q6_K: "Q6_K", Q5_K: "Q5_K"}
+BLOCK = {Q8_0: (32, 34), Q4_0: (32, 18), Q4_K: (256, 144), Q6_K: (256, 210), Q5_K: (256, 176)}
 
 
 def seed_for(name: str, base: int = BASE_SEED) -> int:
@@ -73,7 +74,7 @@ def gen_weights(wtype: int, M: int, K: int, name: str, base: int = BASE_SEED,
         blk[:, :, 2:34] = rng.integers(-127, 128, size=(M, nb, 32), dtype=np.int8).view(np.uint8)
     elif wtype == Q4_0:
         blk[:, :, 0:2] = _f16_bytes(rng.uniform(1e-3, 1e-2, size=(M, nb)))
-    elif wtype == Q4_K:
+    elif wtype in (Q4_K, Q5_K):
         blk[:, :, 0:2] = _f16_bytes(rng.uniform(1e-3, 1e-2, size=(M, nb)))
         blk[:, :, 2:4] = _f16_bytes(rng.uniform(0.0, 1e-2, size=(M, nb)))
     elif wtype == Q6_K:

@@ -32,9 +32,9 @@ _BUILD = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD, "libqmm_oracle.so")
 _SRC = os.path.join(_HERE, "qmm_oracle.c")
 
-Q8_0, Q4_0, Q4_K, Q6_K = 0, 1, 2, 3
+Q8_0, Q4_0, Q4_K, Q6_K, Q5_K = 0, 1, 2, 3, 4
 X_F32, X_BF16 = 0, 1
-BLOCK = {Q8_0: (32, 34), Q4_0: (32, 18), Q4_K: (256, 144), Q6_K: (256, 210)}
+BLOCK = {Q8_0: (32, 34), Q4_0: (32, 18), Q4_K: (256, 144), Q6_K: (256, 210), Q5_K: (256, 176)}
 
 _lock = threading.Lock()
 _lib = None

@@ -17,13 +17,15 @@
 int orc_block_info(int wtype, int *elems, int *bytes) {
     /* Block sizes: "cera 0.5.2 src/backend/cpu.rs" matmul_q4_0_f32 (18 B / 32),
      * matmul_q8_0_f32 (34 B / 32), matmul_q4km_f32 (144 B / 256);
-     * "cera 0.3.1 src/model/gpu_lfm2.rs" weight upload (Q6_K 210 B / 256). */
+     * "cera 0.3.1 src/model/gpu_lfm2.rs" weight upload (Q6_K 210 B / 256,
+     * Q5_K 176 B / 256). */
     int e, b;
     switch (wtype) {
     case ORC_Q8_0: e = 32;  b = 34;  break;
     case ORC_Q4_0: e = 32;  b = 18;  break;
     case ORC_Q4_K: e = 256; b = 144; break;
     case ORC_Q6_K: e = 256; b = 210; break;
+    case ORC_Q5_K: e = 256; b = 176; break;
     default: return -1;
     }
     if (elems) *elems = e;
@@ -128,12 +130,34 @@ static void deq_q6_k(const uint8_t *b, double *out) {
     }
 }
 
+/* Q5_K, 176 bytes.  READING (only the 176-byte size is on the pages): GGUF
+ * order d (f16) @0, dmin (f16) @2, 12 scale bytes @4 (the Q4_K packing),
+ * qh[32] @16, qs[128] @48.  Sub-block s = e/32, l = e%32: the low 4 bits are
+ * Q4_K's nibble (qs[(s/2)*32 + l], low for even s, high for odd s), bit 4 is
+ * bit s of qh[l];  q = low | bit << 4 (0..31),  w = d*sc_s*q - dmin*m_s. */
+static void deq_q5_k(const uint8_t *b, double *out) {
+    double d = orc_f16_to_f64(rd16(b));
+    double dmin = orc_f16_to_f64(rd16(b + 2));
+    const uint8_t *S = b + 4;
+    const uint8_t *qh = b + 16;
+    const uint8_t *qs = b + 48;
+    for (int e = 0; e < 256; ++e) {
+        int s = e / 32, l = e % 32, sc, mn;
+        q4k_scale_min(S, s, &sc, &mn);
+        uint8_t byte = qs[(s / 2) * 32 + l];
+        int lo = (s % 2 == 0) ? (byte & 0x0f) : (byte >> 4);
+        int q = lo | (((qh[l] >> s) & 1) << 4);
+        out[e] = d * (double)sc * (double)q - dmin * (double)mn;
+    }
+}
+
 int orc_dequant_block(int wtype, const uint8_t *blk, double *out) {
     switch (wtype) {
     case ORC_Q8_0: deq_q8_0(blk, out); return 0;
     case ORC_Q4_0: deq_q4_0(blk, out); return 0;
     case ORC_Q4_K: deq_q4_k(blk, out); return 0;
     case ORC_Q6_K: deq_q6_k(blk, out); return 0;
+    case ORC_Q5_K: deq_q5_k(blk, out); return 0;
     default: return -1;
     }
 }

@@ -23,14 +23,16 @@
  *   - "cera 0.3.1 src/model/gpu_lfm2.rs": GpuLfm2Model::new weight upload
  *     (block byte sizes: Q4_K 144 B, Q6_K 210 B per 256 weights).
  * Readings where the pages are silent (Q8_0 field order, Q4_K 6-bit scale
- * packing, Q6_K byte order and bit map) follow the published GGUF/ggml block
- * definitions and are marked READING at the function that uses them.
+ * packing, Q6_K and Q5_K byte order and bit maps) follow the published
+ * GGUF/ggml block definitions and are marked READING at the function that
+ * uses them.
  *
  * Pins: every function here is checked by the CPU test-suite against worked
  * blocks, closed forms, invariants, a library f16 decoder and an independent
  * brute-force path.  The Q4_K scale packing and the Q6_K bit map are pinned
- * only to their READING (no GGUF file is available to compare with): parity
- * unpinned against real GGUF files for those two layouts.
+ * only to their READING (no GGUF file is available to compare with), and so
+ * is the Q5_K layout: parity unpinned against real GGUF files for those
+ * three layouts.
  */
 #ifndef QMM_ORACLE_H
 #define QMM_ORACLE_H
@@ -43,7 +45,7 @@ extern "C" {
 #endif
 
 /* Weight formats, numbered as the library's public enum. */
-enum { ORC_Q8_0 = 0, ORC_Q4_0 = 1, ORC_Q4_K = 2, ORC_Q6_K = 3 };
+enum { ORC_Q8_0 = 0, ORC_Q4_0 = 1, ORC_Q4_K = 2, ORC_Q6_K = 3, ORC_Q5_K = 4 };
 /* Activation element types. */
 enum { ORC_X_F32 = 0, ORC_X_BF16 = 1 };
 

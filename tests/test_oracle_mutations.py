@@ -24,9 +24,13 @@ MUTANTS = {
     "q4_0_offset": ("(double)(nib - 8) * d", "(double)(nib - 7) * d"),
     "q4_0_high_nibble": ("(qs[e - 16] >> 4)", "(qs[e - 16] & 0x0f)"),
     "q8_0_index": ("(int8_t)b[2 + e]", "(int8_t)b[1 + e]"),
-    "q4_k_min_sign": ("- dmin * (double)mn", "+ dmin * (double)mn"),
+    "q4_k_min_sign": ("(byte >> 4);\n        out[e] = d * (double)sc * (double)q - dmin * (double)mn;",
+                      "(byte >> 4);\n        out[e] = d * (double)sc * (double)q + dmin * (double)mn;"),
+    "q5_k_min_sign": ("<< 4);\n        out[e] = d * (double)sc * (double)q - dmin * (double)mn;",
+                      "<< 4);\n        out[e] = d * (double)sc * (double)q + dmin * (double)mn;"),
     "q4_k_scale_hi": ("((S[s - 4] >> 6) << 4)", "((S[s] >> 6) << 4)"),
-    "q4_k_nibble_parity": ("(s % 2 == 0) ? (byte & 0x0f)", "(s % 2 == 1) ? (byte & 0x0f)"),
+    "q4_k_nibble_parity": ("int q = (s % 2 == 0) ? (byte & 0x0f)", "int q = (s % 2 == 1) ? (byte & 0x0f)"),
+    "q5_k_nibble_parity": ("int lo = (s % 2 == 0) ? (byte & 0x0f)", "int lo = (s % 2 == 1) ? (byte & 0x0f)"),
     "q4_k_qs_index": ("qs[(s / 2) * 32 + e % 32]", "qs[s * 16 + e % 16]"),
     "q6_k_qh_shift": ("(qh[32 * h + l] >> (2 * j)) & 3", "(qh[32 * h + l] >> (2 * h)) & 3"),
     "q6_k_scale_index": ("sc[e / 16]", "sc[e / 32]"),
@@ -45,6 +49,9 @@ MUTANTS = {
     "q8act_clamp": ("q > 127.0f ? 127.0f : q", "q > 126.0f ? 126.0f : q"),
     "f16_round_even": ("nearbyint(ldexp(v, 10 - e))", "floor(ldexp(v, 10 - e))"),
     "f16_sign": ("(bits >> 16) & 0x8000u", "(bits >> 17) & 0x8000u"),
+    "q5_k_qh_bit": ("int q = lo | (((qh[l] >> s) & 1) << 4);", "int q = lo | (((qh[l] >> (s / 2)) & 1) << 4);"),
+    "q5_k_qs_offset": ("const uint8_t *qs = b + 48;", "const uint8_t *qs = b + 16;"),
+    "q5_k_high_weight": ("int q = lo | (((qh[l] >> s) & 1) << 4);", "int q = lo | (((qh[l] >> s) & 1) << 3);"),
     "f16_subnormal_round": ("nearbyint(ldexp(v, 24))", "floor(ldexp(v, 24))"),
 }
 
@@ -93,7 +100,7 @@ def _pins_fail(lib) -> list[str]:
     if not np.array_equal(got[ok], ref[ok]):
         failed.append("f16")
     # brute force dequant + textbook matmul
-    for fmt in (synth.Q8_0, synth.Q4_0, synth.Q4_K, synth.Q6_K):
+    for fmt in (synth.Q8_0, synth.Q4_0, synth.Q4_K, synth.Q6_K, synth.Q5_K):
         M, K, N = 4, 512, 2
         raw = synth.gen_weights(fmt, M, K, "mutant")
         x = synth.gen_x(N, K, "mutant")

@@ -22,8 +22,8 @@ import oracle
 from block_quantized_gemv_gguf_gb300 import synth
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
-FMT = {"Q8_0": oracle.Q8_0, "Q4_0": oracle.Q4_0, "Q4_K": oracle.Q4_K, "Q6_K": oracle.Q6_K}
-ALL = [oracle.Q8_0, oracle.Q4_0, oracle.Q4_K, oracle.Q6_K]
+FMT = {"Q8_0": oracle.Q8_0, "Q4_0": oracle.Q4_0, "Q4_K": oracle.Q4_K, "Q6_K": oracle.Q6_K, "Q5_K": oracle.Q5_K}
+ALL = [oracle.Q8_0, oracle.Q4_0, oracle.Q4_K, oracle.Q6_K, oracle.Q5_K]
 
 
 # --------------------------------------------------------------------------
@@ -62,7 +62,7 @@ BLOCK_CASES = _parse_blocks()
 def test_block_sizes_match_pages():
     with open(os.path.join(GOLDEN, "block_sizes.txt")) as f:
         rows = [l.split()[:3] for l in f if l.strip() and not l.startswith("#")]
-    assert len(rows) == 4
+    assert len(rows) == 5
     for fmt, e, b in rows:
         assert oracle.block_info(FMT[fmt]) == (int(e), int(b))
 
@@ -123,6 +123,23 @@ def brute_dequant(fmt: int, raw: np.ndarray, M: int, K: int) -> np.ndarray:
         mn[..., 4:8] = S[..., 8:12] // 16 + (S[..., 4:8] // 64) * 16
         qs = blk[..., 16:144].astype(np.int64).reshape(M, K // E, 4, 32)
         q = np.stack([qs % 16, qs // 16], axis=3).reshape(M, K // E, 8, 32)
+        w = (d[..., None, None] * sc[..., None] * q - dmin[..., None, None] * mn[..., None])
+        w = w.reshape(M, K // E, 256)
+    elif fmt == oracle.Q5_K:
+        d = _np_f16(blk[..., 0:2])
+        dmin = _np_f16(blk[..., 2:4])
+        S = blk[..., 4:16].astype(np.int64)
+        sc = np.empty(S.shape[:-1] + (8,), np.int64)
+        mn = np.empty_like(sc)
+        sc[..., 0:4] = S[..., 0:4] % 64
+        mn[..., 0:4] = S[..., 4:8] % 64
+        sc[..., 4:8] = S[..., 8:12] % 16 + (S[..., 0:4] // 64) * 16
+        mn[..., 4:8] = S[..., 8:12] // 16 + (S[..., 4:8] // 64) * 16
+        qh = blk[..., 16:48].astype(np.int64)                                  # [.., 32]
+        qs = blk[..., 48:176].astype(np.int64).reshape(M, K // E, 4, 32)
+        lo = np.stack([qs % 16, qs // 16], axis=3).reshape(M, K // E, 8, 32)
+        hi = np.stack([(qh >> s) % 2 for s in range(8)], axis=-2)              # [.., 8, 32]
+        q = lo + 16 * hi
         w = (d[..., None, None] * sc[..., None] * q - dmin[..., None, None] * mn[..., None])
         w = w.reshape(M, K // E, 256)
     elif fmt == oracle.Q6_K:
@@ -523,3 +540,29 @@ def test_q8act_matmul_one_hot_closed_form():
 def test_q8act_bad_length_rejected():
     with pytest.raises(ValueError):
         oracle.quantize_q8_0(np.zeros(31, dtype=np.float32))
+
+
+@pytest.mark.parametrize("a,b,q,h", [(1, 0, 0, 0), (5, 3, 7, 1), (63, 63, 15, 1), (17, 40, 9, 0)])
+def test_q5_k_constant_closed_form(a, b, q, h):
+    # every nibble q, every qh bit h: w = d*a*(q + 16h) - dmin*b
+    d, dmin = np.float16(0.0031), np.float16(0.0077)
+    blk = (_f16_le(float(d)) + _f16_le(float(dmin)) + _q4k_scale_bytes([a] * 8, [b] * 8)
+           + bytes([0xFF if h else 0]) * 32 + bytes([q | (q << 4)]) * 128)
+    w = oracle.dequant_block(oracle.Q5_K, blk)
+    assert np.all(w == float(d) * a * (q + 16 * h) - float(dmin) * b)
+
+
+def test_q5_k_single_qh_bit_moves_one_element():
+    # bit s of qh[l] is bit 4 of element 32 s + l, and nothing else
+    base = bytearray(176)
+    base[0:2] = _f16_le(1.0)
+    base[4:16] = _q4k_scale_bytes([1] * 8, [0] * 8)
+    w0 = oracle.dequant_block(oracle.Q5_K, bytes(base))
+    for l in range(32):
+        for s in range(8):
+            blk = bytearray(base)
+            blk[16 + l] = 1 << s
+            w = oracle.dequant_block(oracle.Q5_K, bytes(blk))
+            diff = np.nonzero(w != w0)[0]
+            assert list(diff) == [32 * s + l]
+            assert w[32 * s + l] - w0[32 * s + l] == 16
