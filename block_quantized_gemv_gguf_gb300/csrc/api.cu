@@ -99,6 +99,7 @@ bool block_geom(int wt, int &E, int &B) {
     case QMM_Q4_0: E = 32; B = 18; return true;
     case QMM_Q4_K: E = 256; B = 144; return true;
     case QMM_Q6_K: E = 256; B = 210; return true;
+    case QMM_Q5_K: E = 256; B = 176; return true;
     default: return false;
     }
 }

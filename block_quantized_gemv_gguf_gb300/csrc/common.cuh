@@ -14,13 +14,17 @@ namespace qmm {
 // ---------------------------------------------------------------------------
 // Block geometry (weights / bytes per block) of the four GGUF formats.
 // ---------------------------------------------------------------------------
-enum Fmt : int { Q8_0 = 0, Q4_0 = 1, Q4_K = 2, Q6_K = 3 };
+enum Fmt : int { Q8_0 = 0, Q4_0 = 1, Q4_K = 2, Q6_K = 3, Q5_K = 4 };
 
 template <int F> struct Blk;
 template <> struct Blk<Q8_0> { static constexpr int E = 32;  static constexpr int B = 34;  };
 template <> struct Blk<Q4_0> { static constexpr int E = 32;  static constexpr int B = 18;  };
 template <> struct Blk<Q4_K> { static constexpr int E = 256; static constexpr int B = 144; };
 template <> struct Blk<Q6_K> { static constexpr int E = 256; static constexpr int B = 210; };
+template <> struct Blk<Q5_K> { static constexpr int E = 256; static constexpr int B = 176; };
+
+// Formats with a per-sub-block min term (w = d*sc*q - dmin*m).
+constexpr bool kmin_fmt(int f) { return f == Q4_K || f == Q5_K; }
 
 // Status codes written to the per-device status word (same values as the
 // public qmm_status enum).

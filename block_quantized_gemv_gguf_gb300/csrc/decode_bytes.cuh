@@ -7,6 +7,7 @@
 //   Q4_0  w = (nibble - 8) * d            (exact)
 //   Q4_K  w = fma(d*sc, q, -(dmin*m))     (d*sc, q, dmin*m exact; one rounding)
 //   Q6_K  w = (d*scale) * (q - 32)        (exact, < 24 significant bits)
+//   Q5_K  w = fma(d*sc, q, -(dmin*m))     (as Q4_K, q = nibble | qh bit << 4)
 #pragma once
 
 #include "common.cuh"
@@ -58,6 +59,23 @@ __device__ __forceinline__ void decode_unit(const uint8_t *row, int64_t u, float
 #pragma unroll
         for (int l = 0; l < 32; ++l) {
             const float q = (float)((ldb(qs + l) >> shift) & 15u);
+            w[l] = __fmaf_rn(dsc, q, -dmn);
+        }
+    } else if constexpr (F == Q5_K) {
+        const uint8_t *b = row + (u >> 3) * 176;
+        const int s = (int)(u & 7);
+        const float d = f16_bits(ld16(b));
+        const float dmin = f16_bits(ld16(b + 2));
+        int sc, mn;
+        q4k_scale_min_bytes(b + 4, s, sc, mn);
+        const float dsc = d * (float)sc;
+        const float dmn = dmin * (float)mn;
+        const uint8_t *qh = b + 16;
+        const uint8_t *qs = b + 48 + (s >> 1) * 32;
+        const int shift = (s & 1) * 4;
+#pragma unroll
+        for (int l = 0; l < 32; ++l) {
+            const float q = (float)(((ldb(qs + l) >> shift) & 15u) | (((ldb(qh + l) >> s) & 1u) << 4));
             w[l] = __fmaf_rn(dsc, q, -dmn);
         }
     } else {  // Q6_K

@@ -48,6 +48,7 @@ template <> struct Raw<Q8_0> { static constexpr int bytes = 272; };   // 8 block
 template <> struct Raw<Q4_0> { static constexpr int bytes = 144; };   // 8 blocks of 18
 template <> struct Raw<Q4_K> { static constexpr int bytes = 144; };   // 1 super-block
 template <> struct Raw<Q6_K> { static constexpr int bytes = 240; };   // 210 B + alignment slack
+template <> struct Raw<Q5_K> { static constexpr int bytes = 176; };   // 1 super-block
 
 template <int F, int BN> struct Layout {
     static constexpr int X_BYTES = BN * 128;
@@ -182,6 +183,30 @@ __device__ __forceinline__ void dequant32<Q4_K>(const uint8_t *rb, int sub, int 
 #pragma unroll
     for (int t = 0; t < 8; ++t) {
         const uint32_t v = (words[t] >> sh) & 0x0F0F0F0Fu;
+        o[2 * t] = pack_bf16x2(fmaf(a, byte_as_128_plus<0>(v), c), fmaf(a, byte_as_128_plus<1>(v), c));
+        o[2 * t + 1] = pack_bf16x2(fmaf(a, byte_as_128_plus<2>(v), c), fmaf(a, byte_as_128_plus<3>(v), c));
+    }
+}
+
+// Q5_K: as Q4_K, with bit s of qh[l] as bit 4 of sub-block s's element l.
+template <>
+__device__ __forceinline__ void dequant32<Q5_K>(const uint8_t *rb, int sub, int h, uint32_t (&o)[16]) {
+    const float d = f16_bits(*reinterpret_cast<const uint16_t *>(rb));
+    const float dmin = f16_bits(*reinterpret_cast<const uint16_t *>(rb + 2));
+    const int s = 2 * sub + h;
+    float sc, mn;
+    q4k_sm(rb + 4, s, sc, mn);
+    const float a = d * sc;
+    const float c = -(128.f * a + dmin * mn);
+    const uint4 *qh = reinterpret_cast<const uint4 *>(rb + 16);
+    const uint4 *qs = reinterpret_cast<const uint4 *>(rb + 48 + 32 * sub);
+    const uint4 h0 = qh[0], h1 = qh[1], q0 = qs[0], q1 = qs[1];
+    const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+    const uint32_t hw[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+    const int sh = 4 * h;   // sub-block 2sub: low nibbles, 2sub+1: high nibbles
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+        const uint32_t v = ((words[t] >> sh) & 0x0F0F0F0Fu) | (((hw[t] >> s) & 0x01010101u) << 4);
         o[2 * t] = pack_bf16x2(fmaf(a, byte_as_128_plus<0>(v), c), fmaf(a, byte_as_128_plus<1>(v), c));
         o[2 * t + 1] = pack_bf16x2(fmaf(a, byte_as_128_plus<2>(v), c), fmaf(a, byte_as_128_plus<3>(v), c));
     }
@@ -530,6 +555,7 @@ int gemm_raw_window_bytes(int fmt) {
     case Q4_0: return Raw<Q4_0>::bytes;
     case Q4_K: return Raw<Q4_K>::bytes;
     case Q6_K: return Raw<Q6_K>::bytes;
+    case Q5_K: return Raw<Q5_K>::bytes;
     default: return 0;
     }
 }
@@ -540,6 +566,7 @@ cudaError_t launch_gemm_tc(const GemmArgs &a, const CUtensorMap &wmap, const CUt
     case Q4_0: return launch_fmt<Q4_0>(a, wmap, xmap, st);
     case Q4_K: return launch_fmt<Q4_K>(a, wmap, xmap, st);
     case Q6_K: return launch_fmt<Q6_K>(a, wmap, xmap, st);
+    case Q5_K: return launch_fmt<Q5_K>(a, wmap, xmap, st);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -46,7 +46,7 @@ template <int F, int NT, int CW> struct GL {
     static constexpr int XRAW = 4096 * NT;                     // raw X slice: up to 4NT f32 / 8NT bf16 rows
     static constexpr int STAGE = RAWW;
     static constexpr int XS = 16 * NT * 32 * 8;                // B fragments of one chunk
-    static constexpr int SXB = F == Q4_K ? 8 * 16 * 4 : 0;     // Q4_K sub-block sums of x
+    static constexpr int SXB = kmin_fmt(F) ? 8 * 16 * 4 : 0;   // Q4_K/Q5_K sub-block sums of x
     static constexpr int XSLOT = XS + SXB;
     static constexpr int SCT = ROWS * SCW * 4;                 // scale table (each warp owns its 16 rows)
     static constexpr int OFF_STAGE = 0;
@@ -187,7 +187,7 @@ __device__ __forceinline__ void prep_x(uint2 *xs, float *sx, const uint8_t *xraw
         }
         xs[blk * 32 + 4 * g + t] = make_uint2(b0, b1);
     }
-    if constexpr (F == Q4_K) {
+    if constexpr (kmin_fmt(F)) {
         for (int it = 32 * w + lane; it < 8 * N; it += 32 * CW) {
             const int s = it & 7, n = it >> 3;
             float acc = 0.f;
@@ -223,7 +223,7 @@ __device__ __forceinline__ void prep_scales(float *sct, const uint8_t *raw, int 
             const uint8_t *b = rb + BB * 4 * half;
             st4(row, 4 * half, f16_bits(lds_u16(b)), f16_bits(lds_u16(b + BB)), f16_bits(lds_u16(b + 2 * BB)),
                 f16_bits(lds_u16(b + 3 * BB)));
-        } else if constexpr (F == Q4_K) {
+        } else if constexpr (kmin_fmt(F)) {   // Q4_K, Q5_K: same header fields
             const float d = f16_bits(lds_u16(rb)), dmin = f16_bits(lds_u16(rb + 2));
             const uint32_t w0 = ld32(rb + 4), w1 = ld32(rb + 8), w2 = ld32(rb + 12);
             // bytes: sc[0..3], mn[0..3], sc[4..7], mn[4..7] (GGUF 6-bit packing)
@@ -346,6 +346,48 @@ __device__ __forceinline__ void compute_chunk(float (&acc)[NT][4], const uint8_t
                     mma16816_z(d, a0, bfrag<KSTR, JSTR>(xb, 2 * s, j), zq);
                     mma16816(d, a1, bfrag<KSTR, JSTR>(xb, 2 * s + 1, j));
                     // w = d*sc*q - dmin*m  =>  sum w x = (d sc) sum q x - (dmin m) sum x
+                    acc_scaled(acc[j], d, dsg[s], dsg8[s]);
+                    if constexpr (P == 2) {       // min term once per token (on the hi piece)
+                        const float sxn = sx[s * 16 + 4 * j + t];
+                        acc[j][0] = fmaf(-dmg[s], sxn, acc[j][0]);
+                        acc[j][2] = fmaf(-dmg8[s], sxn, acc[j][2]);
+                    } else {
+                        const float sx0 = sx[s * 16 + 8 * j + 2 * t], sx1 = sx[s * 16 + 8 * j + 2 * t + 1];
+                        ffma2(acc[j][0], acc[j][1], -dmg[s], -dmg[s], sx0, sx1);
+                        ffma2(acc[j][2], acc[j][3], -dmg8[s], -dmg8[s], sx0, sx1);
+                    }
+                }
+            }
+        }
+    } else if constexpr (F == Q5_K) {
+        float dsg[8], dsg8[8], dmg[8], dmg8[8];
+        ld_scales<8>(dsg, sct, r, 0);
+        ld_scales<8>(dsg8, sct, r + 8, 0);
+        ld_scales<8>(dmg, sct, r, 8);
+        ld_scales<8>(dmg8, sct, r + 8, 8);
+        const uint8_t *qg = rg + 48, *qg8 = rg8 + 48;
+        // bit s of qh[l] is bit 4 of sub-block s's element l (l = 4t+i, 16+4t+i)
+        const uint32_t h0g = ld32(rg + 16 + 4 * t), h1g = ld32(rg + 32 + 4 * t);
+        const uint32_t h0g8 = ld32(rg8 + 16 + 4 * t), h1g8 = ld32(rg8 + 32 + 4 * t);
+#pragma unroll
+        for (int pr = 0; pr < 4; ++pr) {            // sub-blocks 2pr (low nibbles), 2pr+1 (high)
+            const uint32_t w0g = ld32(qg + 32 * pr + 4 * t), w1g = ld32(qg + 32 * pr + 16 + 4 * t);
+            const uint32_t w0g8 = ld32(qg8 + 32 * pr + 4 * t), w1g8 = ld32(qg8 + 32 * pr + 16 + 4 * t);
+#pragma unroll
+            for (int hn = 0; hn < 2; ++hn) {
+                const int s = 2 * pr + hn, sh = 4 * hn;
+                const uint32_t c0g = ((w0g >> sh) & 0x0F0F0F0Fu) | (((h0g >> s) & 0x01010101u) << 4);
+                const uint32_t c0g8 = ((w0g8 >> sh) & 0x0F0F0F0Fu) | (((h0g8 >> s) & 0x01010101u) << 4);
+                const uint32_t c1g = ((w1g >> sh) & 0x0F0F0F0Fu) | (((h1g >> s) & 0x01010101u) << 4);
+                const uint32_t c1g8 = ((w1g8 >> sh) & 0x0F0F0F0Fu) | (((h1g8 >> s) & 0x01010101u) << 4);
+                uint32_t a0[4], a1[4];
+                afrag<0x43u>(a0, c0g, c0g8, k128);
+                afrag<0x43u>(a1, c1g, c1g8, k128);
+#pragma unroll
+                for (int j = 0; j < NT; ++j) {
+                    float d[4];
+                    mma16816_z(d, a0, bfrag<KSTR, JSTR>(xb, 2 * s, j), zq);
+                    mma16816(d, a1, bfrag<KSTR, JSTR>(xb, 2 * s + 1, j));
                     acc_scaled(acc[j], d, dsg[s], dsg8[s]);
                     if constexpr (P == 2) {       // min term once per token (on the hi piece)
                         const float sxn = sx[s * 16 + 4 * j + t];
@@ -567,7 +609,7 @@ template <int F, int NC, int CW, int RG> struct GR {
     static constexpr int KSB = NC * 32;                      // fragment bytes per k-step
     static constexpr int MAXC = XRES / (16 * KSB);           // chunks a CTA may own
     static constexpr int ZB = NC < 8 ? 16 * KSB : 0;         // zero fragments (unused columns)
-    static constexpr int SXB = F == Q4_K ? MAXC * 8 * 16 * 4 : 0;   // Q4_K sub-block sums of x
+    static constexpr int SXB = kmin_fmt(F) ? MAXC * 8 * 16 * 4 : 0;   // Q4_K/Q5_K sub-block sums of x
     static constexpr int SCT = ROWS * SCW * 4;
     static constexpr int OFF_STAGE = 0;
     static constexpr int OFF_X = S * STAGE;
@@ -712,7 +754,7 @@ __global__ void __launch_bounds__(GR<F, NC, CW, RG>::THREADS, GR<F, NC, CW, RG>:
                 }
             }
         }
-        if constexpr (F == Q4_K) {
+        if constexpr (kmin_fmt(F)) {
             // ssx[c][s][n] = sum of x[n] over sub-block s of local chunk c (separate area)
             for (int it = tid; it < nloc * 128; it += CW * 32) {
                 const int n = it & 15, sb = (it >> 4) & 7, c = it >> 7;
@@ -885,6 +927,7 @@ int gemv_window_bytes(int fmt) {
     case Q4_0: return GWin<Q4_0>::bytes;
     case Q4_K: return GWin<Q4_K>::bytes;
     case Q6_K: return GWin<Q6_K>::bytes;
+    case Q5_K: return GWin<Q5_K>::bytes;
     default: return 0;
     }
 }
@@ -927,6 +970,7 @@ cudaError_t launch_gemv_mma(int fmt, const GemvPlan &plan, const GemvSegs &segs,
     case Q4_0: return xbf16 ? launch_f<Q4_0, true>(c) : launch_f<Q4_0, false>(c);
     case Q4_K: return xbf16 ? launch_f<Q4_K, true>(c) : launch_f<Q4_K, false>(c);
     case Q6_K: return xbf16 ? launch_f<Q6_K, true>(c) : launch_f<Q6_K, false>(c);
+    case Q5_K: return xbf16 ? launch_f<Q5_K, true>(c) : launch_f<Q5_K, false>(c);
     default: return cudaErrorInvalidValue;
     }
 }

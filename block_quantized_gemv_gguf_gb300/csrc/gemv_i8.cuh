@@ -80,7 +80,7 @@ template <int F, int MODE, int NTOK, bool XBF16, int CW, int RG> struct GI {
     static constexpr int FRAG_C = 8 * NT * NCW * 32;
     static constexpr int CI_C = CI ? 8 * NT * 64 : 0;
     static constexpr int XS_C = FOLD ? 8 * 4 : 8 * NT * 32;
-    static constexpr int SX_C = F == Q4_K ? 8 * 16 * 4 : 0;
+    static constexpr int SX_C = kmin_fmt(F) ? 8 * 16 * 4 : 0;
     static constexpr int PER_C = RAW_C + FRAG_C + CI_C + XS_C + SX_C;
     static constexpr int rup(int v, int a) { return (v + a - 1) / a * a; }
     // fixed areas first; the X areas after them are sized at launch for the
@@ -238,8 +238,8 @@ __device__ __forceinline__ void prep_x_i8(const uint8_t *sraw, int kslice, int N
             if constexpr (H == 1) s += __shfl_xor_sync(0xffffffffu, s, 4);
             ds[j] = s;
         }
-        float bsum = 0.f;   // Q4_K: sum of the represented x over the block
-        if constexpr (F == Q4_K) {
+        float bsum = 0.f;   // Q4_K/Q5_K: sum of the represented x over the block
+        if constexpr (kmin_fmt(F)) {
 #pragma unroll
             for (int j = 0; j < D; ++j) bsum += __uint_as_float((uint32_t)(127 - 8 * j) << 23) * (float)ds[j];
             bsum *= scale;
@@ -266,7 +266,7 @@ __device__ __forceinline__ void prep_x_i8(const uint8_t *sraw, int kslice, int N
             }
             if (grp == 0) {
                 if constexpr (L::FOLD) xs[blk] = scale;
-                if constexpr (F == Q4_K) sx[blk * 16 + n] = bsum;
+                if constexpr (kmin_fmt(F)) sx[blk * 16 + n] = bsum;
             }
         }
     }
@@ -291,7 +291,7 @@ __device__ __forceinline__ void prep_scales_i8(float *sct, const uint8_t *raw, i
         const int b0 = 4 * half;
         st4(row, b0, f16_bits(lds_u16(b)) * xf(b0), f16_bits(lds_u16(b + BB)) * xf(b0 + 1),
             f16_bits(lds_u16(b + 2 * BB)) * xf(b0 + 2), f16_bits(lds_u16(b + 3 * BB)) * xf(b0 + 3));
-    } else if constexpr (F == Q4_K) {
+    } else if constexpr (kmin_fmt(F)) {   // Q4_K, Q5_K: same header fields
         const float d = f16_bits(lds_u16(rb)), dmin = f16_bits(lds_u16(rb + 2));
         const uint32_t w0 = ld32(rb + 4), w1 = ld32(rb + 8), w2 = ld32(rb + 12);
         // bytes: sc[0..3], mn[0..3], sc[4..7], mn[4..7] (GGUF 6-bit packing)
@@ -451,6 +451,42 @@ __device__ __forceinline__ void compute_chunk_i8(float (&acc)[NT][4], const uint
                                                                     make_float2(dsg8[s], 0.f));
                     // w = d sc q - dmin m  =>  - dmin m * (sum of x over the sub-block), once per
                     // token, on the slot of the token's first column
+                    const float x0 = mmsk[j][0] != 0.f ? sx[s * 16 + mtok[j][0]] : 0.f;
+                    acc[j][0] = fmaf(-dmg[s], x0, acc[j][0]);
+                    acc[j][2] = fmaf(-dmg8[s], x0, acc[j][2]);
+                    if constexpr (MODE == XM_Q8) {
+                        const float x1 = mmsk[j][1] != 0.f ? sx[s * 16 + mtok[j][1]] : 0.f;
+                        acc[j][1] = fmaf(-dmg[s], x1, acc[j][1]);
+                        acc[j][3] = fmaf(-dmg8[s], x1, acc[j][3]);
+                    }
+                }
+            }
+        }
+    } else if constexpr (F == Q5_K) {
+        float dsg[8], dsg8[8], dmg[8], dmg8[8];
+        ld_scales<8>(dsg, sct, r, 0);
+        ld_scales<8>(dsg8, sct, r + 8, 0);
+        ld_scales<8>(dmg, sct, r, 8);
+        ld_scales<8>(dmg8, sct, r + 8, 8);
+        const uint8_t *qg = rg + 48, *qg8 = rg8 + 48;
+        // bit s of qh[l] is bit 4 of sub-block s's element l
+        const uint32_t h0g = ld32(rg + 16 + 4 * t), h1g = ld32(rg + 32 + 4 * t);
+        const uint32_t h0g8 = ld32(rg8 + 16 + 4 * t), h1g8 = ld32(rg8 + 32 + 4 * t);
+#pragma unroll
+        for (int pr = 0; pr < 4; ++pr) {            // sub-blocks 2pr (low nibbles), 2pr+1 (high)
+            const uint32_t w0g = ld32(qg + 32 * pr + 4 * t), w1g = ld32(qg + 32 * pr + 16 + 4 * t);
+            const uint32_t w0g8 = ld32(qg8 + 32 * pr + 4 * t), w1g8 = ld32(qg8 + 32 * pr + 16 + 4 * t);
+#pragma unroll
+            for (int hn = 0; hn < 2; ++hn) {
+                const int s = 2 * pr + hn, sh = 4 * hn;
+                const uint32_t a[4] = {((w0g >> sh) & M4) | (((h0g >> s) & 0x01010101u) << 4),
+                                       ((w0g8 >> sh) & M4) | (((h0g8 >> s) & 0x01010101u) << 4),
+                                       ((w1g >> sh) & M4) | (((h1g >> s) & 0x01010101u) << 4),
+                                       ((w1g8 >> sh) & M4) | (((h1g8 >> s) & 0x01010101u) << 4)};
+#pragma unroll
+                for (int j = 0; j < NT; ++j) {
+                    imma_step<MODE, 1, false, false, FOLD, NT, NCW>(acc[j], a, xv, s, j, make_float2(dsg[s], 0.f),
+                                                                    make_float2(dsg8[s], 0.f));
                     const float x0 = mmsk[j][0] != 0.f ? sx[s * 16 + mtok[j][0]] : 0.f;
                     acc[j][0] = fmaf(-dmg[s], x0, acc[j][0]);
                     acc[j][2] = fmaf(-dmg8[s], x0, acc[j][2]);

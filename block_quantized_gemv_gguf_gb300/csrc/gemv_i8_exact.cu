@@ -47,6 +47,7 @@ int gemv_i8_exact_maxc(int fmt, int N, int xbf16, int rows, int rg) {
     case Q4_0: return maxc_f<Q4_0>(N, xbf16, rows, rg);
     case Q4_K: return maxc_f<Q4_K>(N, xbf16, rows, rg);
     case Q6_K: return maxc_f<Q6_K>(N, xbf16, rows, rg);
+    case Q5_K: return maxc_f<Q5_K>(N, xbf16, rows, rg);
     default: return 0;
     }
 }
@@ -67,6 +68,8 @@ cudaError_t launch_gemv_i8_exact(int fmt, const GemvPlan &plan, const GemvSegs &
                             : exact_n<Q4_K, false>(plan, segs, xin, K, N, pdl, status, limit, st, amax);
     case Q6_K: return xbf16 ? exact_n<Q6_K, true>(plan, segs, xin, K, N, pdl, status, limit, st, amax)
                             : exact_n<Q6_K, false>(plan, segs, xin, K, N, pdl, status, limit, st, amax);
+    case Q5_K: return xbf16 ? exact_n<Q5_K, true>(plan, segs, xin, K, N, pdl, status, limit, st, amax)
+                            : exact_n<Q5_K, false>(plan, segs, xin, K, N, pdl, status, limit, st, amax);
     default: return cudaErrorInvalidValue;
     }
 }

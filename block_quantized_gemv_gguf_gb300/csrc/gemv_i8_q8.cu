@@ -96,6 +96,7 @@ int gemv_i8_q8_maxc(int fmt, int N, int rows) {
     case Q4_0: return maxc_f<Q4_0>(N, rows);
     case Q4_K: return maxc_f<Q4_K>(N, rows);
     case Q6_K: return maxc_f<Q6_K>(N, rows);
+    case Q5_K: return maxc_f<Q5_K>(N, rows);
     default: return 0;
     }
 }
@@ -112,6 +113,7 @@ cudaError_t launch_gemv_i8_q8(int fmt, const GemvPlan &plan, const GemvSegs &seg
     case Q4_0: return q8_n<Q4_0>(plan, segs, xin, K, N, pdl, status, limit, st, amax);
     case Q4_K: return q8_n<Q4_K>(plan, segs, xin, K, N, pdl, status, limit, st, amax);
     case Q6_K: return q8_n<Q6_K>(plan, segs, xin, K, N, pdl, status, limit, st, amax);
+    case Q5_K: return q8_n<Q5_K>(plan, segs, xin, K, N, pdl, status, limit, st, amax);
     default: return cudaErrorInvalidValue;
     }
 }

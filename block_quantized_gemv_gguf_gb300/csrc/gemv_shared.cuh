@@ -28,6 +28,7 @@ template <> struct GWin<Q8_0> { static constexpr int bytes = 272; };
 template <> struct GWin<Q4_0> { static constexpr int bytes = 144; };
 template <> struct GWin<Q4_K> { static constexpr int bytes = 144; };
 template <> struct GWin<Q6_K> { static constexpr int bytes = 240; };
+template <> struct GWin<Q5_K> { static constexpr int bytes = 176; };
 
 __device__ __forceinline__ uint16_t lds_u16(const uint8_t *p) { return *reinterpret_cast<const uint16_t *>(p); }
 __device__ __forceinline__ uint32_t ld32(const uint8_t *p) { return *reinterpret_cast<const uint32_t *>(p); }

@@ -103,6 +103,7 @@ cudaError_t launch_dequant(int fmt, const uint8_t *W, int64_t M, int64_t K, floa
     case Q4_0: dequant_kernel<Q4_0><<<g, 256, 0, st>>>(W, M, K, out); break;
     case Q4_K: dequant_kernel<Q4_K><<<g, 256, 0, st>>>(W, M, K, out); break;
     case Q6_K: dequant_kernel<Q6_K><<<g, 256, 0, st>>>(W, M, K, out); break;
+    case Q5_K: dequant_kernel<Q5_K><<<g, 256, 0, st>>>(W, M, K, out); break;
     default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
@@ -125,6 +126,7 @@ cudaError_t launch_gemv_generic(int fmt, const uint8_t *W, int64_t M, int64_t K,
     case Q4_0: gemv_generic_dispatch<Q4_0>(W, M, K, X, xbf16, N, Y, st); break;
     case Q4_K: gemv_generic_dispatch<Q4_K>(W, M, K, X, xbf16, N, Y, st); break;
     case Q6_K: gemv_generic_dispatch<Q6_K>(W, M, K, X, xbf16, N, Y, st); break;
+    case Q5_K: gemv_generic_dispatch<Q5_K>(W, M, K, X, xbf16, N, Y, st); break;
     default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

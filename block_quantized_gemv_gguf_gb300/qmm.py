@@ -20,11 +20,11 @@ import torch
 
 from . import build as _build
 
-Q8_0, Q4_0, Q4_K, Q6_K = 0, 1, 2, 3
+Q8_0, Q4_0, Q4_K, Q6_K, Q5_K = 0, 1, 2, 3, 4
 X_F32, X_BF16 = 0, 1
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = 0, 1, 2, 3, 4
 GEMV_MAX_N, GEMM_MAX_N = 16, 512
-BLOCK = {Q8_0: (32, 34), Q4_0: (32, 18), Q4_K: (256, 144), Q6_K: (256, 210)}
+BLOCK = {Q8_0: (32, 34), Q4_0: (32, 18), Q4_K: (256, 144), Q6_K: (256, 210), Q5_K: (256, 176)}
 EXPORTS = ("qmm_gemv", "qmm_gemv_argmax", "qmm_gemv_multi", "qmm_gemm", "qmm_gemm_workspace_bytes", "qmm_matmul", "qmm_matmul_host",
            "qmm_dequant", "qmm_block_info", "qmm_last_device_error", "qmm_status_str",
            "qmm_set_wait_limit", "qmm_set_static_weights", "qmm_set_gemv_i8", "qmm_quantize_q8_0",

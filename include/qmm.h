@@ -31,6 +31,11 @@
  *          j >= 2) and bits 2j..2j+1 of qh[32h + l] as bits 4..5;
  *          w = d * scales[e/16] * (q - 32) (GGUF layout; the 210-byte size is
  *          "cera 0.3.1 src/model/gpu_lfm2.rs", weight upload).
+ *   Q5_K   176 B / 256 weights: f16 d @0, f16 dmin @2, 12 scale bytes @4
+ *          (packed as Q4_K), qh[32] @16, qs[128] @48; weight e = 32s + l
+ *          takes Q4_K's nibble of qs[(s/2)*32 + l] and bit s of qh[l] as
+ *          bit 4; w = d*sc_s*q - dmin*m_s (GGUF layout; the 176-byte size is
+ *          "cera 0.3.1 src/model/gpu_lfm2.rs", weight upload).
  *   X      [N, K] row-major, f32 or bf16, device memory.
  *   Y      [N, M] row-major f32, device memory, OVERWRITTEN (not accumulated,
  *          as the scalar row loops assign their sum).
@@ -75,7 +80,7 @@
 extern "C" {
 #endif
 
-typedef enum { QMM_Q8_0 = 0, QMM_Q4_0 = 1, QMM_Q4_K = 2, QMM_Q6_K = 3 } qmm_wtype;
+typedef enum { QMM_Q8_0 = 0, QMM_Q4_0 = 1, QMM_Q4_K = 2, QMM_Q6_K = 3, QMM_Q5_K = 4 } qmm_wtype;
 typedef enum { QMM_X_F32 = 0, QMM_X_BF16 = 1 } qmm_xtype;
 typedef enum {
     QMM_OK = 0,

@@ -62,7 +62,8 @@ def _check(wt, w, M, K, x, xbf16=False, rows_for_oracle=None):
     return idx
 
 
-@pytest.mark.parametrize("wt", [synth.Q8_0, synth.Q4_0, synth.Q4_K, synth.Q6_K], ids=["Q8_0", "Q4_0", "Q4_K", "Q6_K"])
+@pytest.mark.parametrize("wt", [synth.Q8_0, synth.Q4_0, synth.Q4_K, synth.Q6_K, synth.Q5_K],
+                         ids=["Q8_0", "Q4_0", "Q4_K", "Q6_K", "Q5_K"])
 @pytest.mark.parametrize("M,K,N", [(300, 4096, 1), (1024, 2048, 2), (4000, 4096, 5), (777, 2048, 8), (20000, 2048, 16)])
 def test_argmax_matches_gemv_and_oracle(wt, M, K, N):
     w = synth.gen_weights(wt, M, K, "amax")

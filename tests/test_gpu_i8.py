@@ -60,7 +60,7 @@ SHAPES = [(64, 256), (200, 1024), (1000, 2048), (4096, 4096), (777, 14336), (400
 @pytest.mark.parametrize("MK", SHAPES, ids=[f"{m}x{k}" for m, k in SHAPES])
 def test_parity_f32(wt, MK):
     M, K = MK
-    if wt in (synth.Q4_K, synth.Q6_K) and K % 256:
+    if wt in (synth.Q4_K, synth.Q6_K, synth.Q5_K) and K % 256:
         pytest.skip("K-quants need K % 256 == 0")
     w = synth.gen_weights(wt, M, K, f"i8-{M}x{K}")
     for N in range(1, max_n(wt) + 1):

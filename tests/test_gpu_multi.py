@@ -50,7 +50,7 @@ def _run(wt, Ms, K, N, tag, unaligned=None, xbf16=False):
         assert np.all(np.abs(y - Y1.cpu().numpy()) <= 2 * (TOL[0] * S + TOL[1]))
 
 
-@pytest.mark.parametrize("wt", [synth.Q8_0, synth.Q4_0, synth.Q4_K, synth.Q6_K], ids=["Q8_0", "Q4_0", "Q4_K", "Q6_K"])
+@pytest.mark.parametrize("wt", [synth.Q8_0, synth.Q4_0, synth.Q4_K, synth.Q6_K, synth.Q5_K], ids=["Q8_0", "Q4_0", "Q4_K", "Q6_K", "Q5_K"])
 @pytest.mark.parametrize("N", [1, 2, 5, 16])
 def test_qkv_like(wt, N):
     _run(wt, [512, 128, 128], 2048, N, f"qkv-{wt}-{N}")

@@ -19,7 +19,7 @@ pytestmark = pytest.mark.gpu
 
 GEMV_TOL = (1e-5, 1e-6)
 GEMM_TOL = (2e-3, 1e-5)
-ALL = [synth.Q8_0, synth.Q4_0, synth.Q4_K, synth.Q6_K]
+ALL = [synth.Q8_0, synth.Q4_0, synth.Q4_K, synth.Q6_K, synth.Q5_K]
 IDS = [synth.NAMES[f] for f in ALL]
 GUARD = 256  # floats of poison on each side of every output
 POISON = 0x7FC0DEAD
@@ -97,7 +97,7 @@ def _edge_blocks(wt, M, K):
         k = i % len(specials)
         if wt in (synth.Q8_0, synth.Q4_0):
             w[r, b, 0:2] = sp[k]
-        elif wt == synth.Q4_K:
+        elif wt in (synth.Q4_K, synth.Q5_K):
             w[r, b, 0:2] = sp[k]
             w[r, b, 2:4] = sp[(k + 3) % len(specials)]
         else:

@@ -21,7 +21,7 @@ import numpy as np, torch, oracle
 from block_quantized_gemv_gguf_gb300 import qmm, synth
 qmm.load()
 bad = []
-for wt in (synth.Q8_0, synth.Q4_0, synth.Q4_K, synth.Q6_K):
+for wt in (synth.Q8_0, synth.Q4_0, synth.Q4_K, synth.Q6_K, synth.Q5_K):
     for (M, K) in ((300, 4096), (77, 2048)):
         w = synth.gen_weights(wt, M, K, "tune")
         W = torch.from_numpy(w).cuda()
