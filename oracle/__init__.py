@@ -188,6 +188,27 @@ def matmul_q8act(wtype: int, w: np.ndarray, M: int, K: int, x: np.ndarray, rows=
     return matmul(wtype, w, M, K, dequant_q8_0_act(scales, quants), rows=rows, nthreads=nthreads)
 
 
+def swiglu(Yg: np.ndarray, Sg: np.ndarray, Yu: np.ndarray, Su: np.ndarray, rel: float, abs_: float):
+    """Fused gate/up activation ("cera 0.5.2 src/backend/cpu.rs",
+    gemv_q4_0_gate_up_swiglu_with_q8: out = silu(gate . x) * (up . x), and
+    silu_mul_inplace: silu(v) = v * sigmoid(v) = v / (1 + exp(-v))), in
+    double on the exact projections.  Returns (out, bound): bound carries
+    a per-projection error rel * S + abs through the activation to first
+    order, |silu'(g) u| e_g + |silu(g)| e_u, plus 1e-6 of |out| for the f32
+    evaluation of the activation itself."""
+    g = np.asarray(Yg, dtype=np.float64)
+    u = np.asarray(Yu, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        sig = 1.0 / (1.0 + np.exp(-g))
+    silu = g * sig
+    out = silu * u
+    dsilu = sig * (1.0 + g * (1.0 - sig))
+    eg = rel * np.asarray(Sg) + abs_
+    eu = rel * np.asarray(Su) + abs_
+    bound = np.abs(dsilu * u) * eg + np.abs(silu) * eu + eg * eu + 1e-6 * np.abs(out) + 1e-7
+    return out, bound
+
+
 def within(y: np.ndarray, Y: np.ndarray, S: np.ndarray, rel: float, abs_: float):
     """Element-wise tolerance test |y - Y| <= rel*S + abs; returns (ok, worst ratio)."""
     err = np.abs(y.astype(np.float64) - Y)

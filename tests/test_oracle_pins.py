@@ -566,3 +566,28 @@ def test_q5_k_single_qh_bit_moves_one_element():
             diff = np.nonzero(w != w0)[0]
             assert list(diff) == [32 * s + l]
             assert w[32 * s + l] - w0[32 * s + l] == 16
+
+
+def test_swiglu_against_library_sigmoid():
+    # silu(g) * u against scipy's logistic function, over a wide range of g
+    special = pytest.importorskip("scipy.special")
+    g = np.concatenate([np.linspace(-60, 60, 241), [0.0, -1e-8, 1e-8, 700.0, -700.0]])
+    u = np.linspace(-3, 3, g.size)
+    out, _ = oracle.swiglu(g, np.zeros_like(g), u, np.zeros_like(u), 0.0, 0.0)
+    ref = g * special.expit(g) * u
+    assert np.allclose(out, ref, rtol=1e-14, atol=1e-300)
+    assert out[g.size - 2] == 700.0 * u[g.size - 2]          # sigmoid(700) == 1 in double
+
+
+def test_swiglu_bound_covers_perturbations():
+    # the first-order bound holds for worst-case perturbations of g and u
+    rng = np.random.default_rng(3)
+    g = rng.normal(0, 4, 2000)
+    u = rng.normal(0, 2, 2000)
+    S = np.abs(rng.normal(0, 30, 2000))
+    out, bound = oracle.swiglu(g, S, u, S, 1e-5, 1e-6)
+    e = 1e-5 * S + 1e-6
+    for sg in (-1, 1):
+        for su in (-1, 1):
+            p, _ = oracle.swiglu(g + sg * e, S, u + su * e, S, 0.0, 0.0)
+            assert np.all(np.abs(p - out) <= bound)
