@@ -519,6 +519,29 @@ qmm_status qmm_last_device_error(void *stream) {
 
 void qmm_set_static_weights(int on) { g_static_weights.store(on ? 1 : 0); }
 
+qmm_status qmm_gemv_swiglu(qmm_wtype wt, const void *Wg, size_t wg_bytes, const void *Wu, size_t wu_bytes,
+                           int64_t M, int64_t K, const void *X, qmm_xtype xt, int64_t N, float *Y, void *workspace,
+                           size_t ws_bytes, void *stream) {
+    int E, B;
+    qmm_status s = validate(wt, Wg, wg_bytes, M, K, X, xt, N, Y, QMM_GEMV_MAX_N, E, B);
+    if (s != QMM_OK) return s;
+    s = validate(wt, Wu, wu_bytes, M, K, X, xt, N, Y, QMM_GEMV_MAX_N, E, B);
+    if (s != QMM_OK) return s;
+    const size_t ny = (size_t)N * (size_t)M;
+    if (!workspace || ws_bytes < 2 * ny * 4 || (uintptr_t)workspace % 16) return QMM_ERR_INVALID_ARG;
+    const size_t wb = (size_t)M * (size_t)(K / E) * (size_t)B;
+    const size_t xs = xt == QMM_X_F32 ? 4 : 2;
+    if (overlaps(workspace, 2 * ny * 4, Wg, wb) || overlaps(workspace, 2 * ny * 4, Wu, wb) ||
+        overlaps(workspace, 2 * ny * 4, X, (size_t)N * K * xs) || overlaps(workspace, 2 * ny * 4, Y, ny * 4))
+        return QMM_ERR_INVALID_ARG;
+    float *g = static_cast<float *>(workspace);
+    float *u = g + ny;
+    const SegIn seg[2] = {{Wg, wg_bytes, M, g}, {Wu, wu_bytes, M, u}};
+    s = gemv_segments(wt, seg, 2, K, X, xt, N, stream);
+    if (s != QMM_OK) return s;
+    return from_cuda(launch_swiglu(g, u, (int64_t)ny, Y, true, static_cast<cudaStream_t>(stream)));
+}
+
 void qmm_set_gemv_i8(int on) { g_gemv_i8.store(on < 0 ? -1 : (on ? 1 : 0)); }
 
 size_t qmm_q8act_workspace_bytes(int64_t N, int64_t K) {

@@ -90,6 +90,20 @@ __global__ void x_to_bf16_kernel(const float *__restrict__ X, int64_t count, __n
     }
 }
 
+// out[i] = silu(g[i]) * u[i], silu(v) = v / (1 + exp(-v)) ("cera 0.5.2
+// src/backend/cpu.rs", silu_mul_inplace: the SwiGLU product of the gate and
+// up projections).  exp overflows to infinity for v < -88, where the
+// quotient is -0: the exact value is below 1e-36 * |v|.
+__global__ void swiglu_kernel(const float *__restrict__ g, const float *__restrict__ u, int64_t count,
+                              float *__restrict__ out) {
+    pdl_launch_dependents();
+    pdl_wait();   // g and u come from the preceding kernel
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < count; i += (int64_t)gridDim.x * blockDim.x) {
+        const float v = g[i];
+        out[i] = v / (1.0f + expf(-v)) * u[i];
+    }
+}
+
 static int grid_for(int64_t work, int per_block) {
     int64_t g = (work + per_block - 1) / per_block;
     if (g > (1 << 20)) g = 1 << 20;
@@ -144,6 +158,26 @@ cudaError_t launch_x_to_bf16(const float *X, int64_t count, uint16_t *out, bool 
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, x_to_bf16_kernel, X, count, reinterpret_cast<__nv_bfloat16 *>(out));
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+}  // namespace qmm
+
+namespace qmm {
+
+cudaError_t launch_swiglu(const float *g, const float *u, int64_t count, float *out, bool pdl, cudaStream_t st) {
+    if (count <= 0) return cudaSuccess;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid_for(count, 256), 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, swiglu_kernel, g, u, count, out);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

@@ -85,6 +85,10 @@ cudaError_t launch_quantize_q8_0(const void *X, int xbf16, int64_t count, float 
 // max_cps chunks; force > 0 requests a split.  0: no split fits max_cps.
 int plan_ks_host(int64_t tiles, int nchunks, int num_sms, int max_cps, int force);
 
+// out[i] = silu(g[i]) * u[i] for i < count.  pdl: programmatic dependent
+// of the preceding kernel (which writes g and u).
+cudaError_t launch_swiglu(const float *g, const float *u, int64_t count, float *out, bool pdl, cudaStream_t st);
+
 // Raw bytes of one 256-weight chunk of a row in the GEMV's staging.
 int gemv_window_bytes(int fmt);
 

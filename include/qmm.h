@@ -276,6 +276,23 @@ QMM_API void qmm_set_static_weights(int on);
 QMM_API void qmm_set_wait_limit(uint64_t cycles);
 
 /*
+ * Gate/up projections with the SwiGLU product ("cera 0.5.2
+ * src/backend/cpu.rs", gemv_q4_0_gate_up_swiglu_with_q8 and
+ * silu_mul_inplace):  Y[n, m] = silu(g) * u,  g = sum_k x(n,k) wg(m,k),
+ * u = sum_k x(n,k) wu(m,k),  silu(v) = v / (1 + exp(-v)).  Wg and Wu are two
+ * M x K matrices of format wt sharing X; 1 <= N <= 16.  Both projections run
+ * in one launch of the fused GEMV (qmm_gemv_multi), writing g and u to
+ * `workspace` (device, 16-byte aligned, >= 2 * N * M * 4 bytes: g [N][M]
+ * then u [N][M], left there), and a second kernel, a programmatic dependent
+ * of the first, writes Y [N][M].  g and u meet the qmm_gemv tolerance; Y
+ * carries it through the activation (plus f32 rounding of exp and the
+ * quotient).  No buffer may overlap another.
+ */
+QMM_API qmm_status qmm_gemv_swiglu(qmm_wtype wt, const void *Wg, size_t wg_bytes, const void *Wu,
+                                   size_t wu_bytes, int64_t M, int64_t K, const void *X, qmm_xtype xt,
+                                   int64_t N, float *Y, void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * GEMV kernel choice for 1 <= N <= 2 (Q6_K: N == 1): on (1, or QMM_GEMV_I8=1
  * in the environment) runs the integer tensor-core kernel, which feeds X to
  * mma.sync as exact int8 digits (per

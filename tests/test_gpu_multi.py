@@ -80,3 +80,43 @@ def test_multi_errors():
     # an output overlapping another output
     assert qmm.qmm_gemv_multi(wt, [(W, 64, Y), (W, 64, Y)], K, X, N) == qmm.ERR_INVALID_ARG
     torch.cuda.synchronize()
+
+
+# ---------------------------------------------------------------------------
+# gate/up with the SwiGLU product (qmm_gemv_swiglu)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("wt", [synth.Q8_0, synth.Q4_0, synth.Q4_K, synth.Q6_K, synth.Q5_K],
+                         ids=["Q8_0", "Q4_0", "Q4_K", "Q6_K", "Q5_K"])
+@pytest.mark.parametrize("N", [1, 4, 16])
+def test_swiglu_parity(wt, N):
+    M, K = 1408, 4096
+    wg = synth.gen_weights(wt, M, K, "swiglu-gate")
+    wu = synth.gen_weights(wt, M, K, "swiglu-up")
+    x = synth.gen_x(N, K, f"swiglu-{N}") * np.float32(3.0)    # gate values across silu's curve
+    X = torch.from_numpy(x).cuda()
+    ws = torch.full((2 * N * M,), float("nan"), device="cuda")
+    Y = qmm.gemv_swiglu(wt, torch.from_numpy(wg).cuda(), torch.from_numpy(wu).cuda(), M, K, X, workspace=ws)
+    torch.cuda.synchronize()
+    Yg, Sg = oracle.matmul(wt, wg, M, K, x)
+    Yu, Su = oracle.matmul(wt, wu, M, K, x)
+    out, bound = oracle.swiglu(Yg, Sg, Yu, Su, *TOL)
+    y = Y.cpu().numpy()
+    err = np.abs(y - out)
+    assert np.all(err <= bound), float(np.max(err / bound))
+    # the projections stay in the workspace and meet the GEMV bar
+    g = ws[: N * M].view(N, M).cpu().numpy()
+    u = ws[N * M:].view(N, M).cpu().numpy()
+    assert oracle.within(g, Yg, Sg, *TOL)[0] and oracle.within(u, Yu, Su, *TOL)[0]
+
+
+def test_swiglu_errors():
+    wt, M, K, N = synth.Q4_0, 64, 512, 2
+    Wg = torch.from_numpy(synth.gen_weights(wt, M, K, "sw-err-g")).cuda()
+    Wu = torch.from_numpy(synth.gen_weights(wt, M, K, "sw-err-u")).cuda()
+    X = torch.from_numpy(synth.gen_x(N, K, "sw-err")).cuda()
+    Y = torch.empty(N, M, device="cuda")
+    ws = torch.empty(2 * N * M, device="cuda")
+    assert qmm.qmm_gemv_swiglu(wt, Wg, Wu, M, K, X, N, Y, ws[: N * M]) == qmm.ERR_INVALID_ARG   # too small
+    assert qmm.qmm_gemv_swiglu(wt, Wg, Wu, M, K, X, N, ws[:N * M].view(N, M), ws) == qmm.ERR_INVALID_ARG  # Y in ws
+    assert qmm.qmm_gemv_swiglu(wt, Wg, Wu, M, K, X, 17, Y, ws) == qmm.ERR_INVALID_ARG
+    torch.cuda.synchronize()
