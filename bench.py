@@ -7,7 +7,8 @@ is its effective HBM bandwidth (algorithmic bytes / device time, GB/s).
 One step runs the whole hot path once over one batch of synthetic input:
   decode   4 x Q4_0 GEMV, N=1                          (decode GEMV)
   lmhead   Q6_K 128256 x 4096 LM head, N=8, f32 X     (small-N GEMV)
-  prefill  Q4_K 4096x4096 and 14336x4096, N=512, f32 X (x->bf16 + tcgen05 GEMM)
+  prefill      Q4_K 4096x4096 and 14336x4096, N=512, bf16 X (tcgen05 GEMM)
+  prefill_f32  the same with f32 X (x->bf16 conversion + tcgen05 GEMM)
 Weights are replicated into R device copies whose total size exceeds L2
 several times, and step s uses copy s % R (rotating inputs > L2 instead of an
 L2 flush).  Each op is captured in a CUDA graph over all R copies and timed
@@ -42,7 +43,7 @@ PREFILL_N = 512
 METRIC = "decode GEMV effective HBM GB/s (% of 8 TB/s); prefill N=512 GEMM TFLOP/s (% peak)"
 WORKLOAD = ("Q4_0 decode GEMV N=1 on Llama-3-8B projection shapes (4096,4096) (1024,4096) (14336,4096) "
             "(4096,14336); same step also runs the Q6_K 128256x4096 LM head at N=8 and the Q4_K "
-            "(4096,4096)+(14336,4096) prefill GEMM at N=512")
+            "(4096,4096)+(14336,4096) prefill GEMM at N=512 with bf16 X and with f32 X")
 NOMINAL_HBM_GBS = 8000.0
 
 
@@ -59,9 +60,9 @@ def peaks():
 # sha256 of the kernel sources they were taken on.  A source change since the
 # capture turns the figure into null.
 TRAFFIC = {
-    # gemv_mma_kernel, Q6_K 128256x4096, N=8: 449.65 MB read + 5.56 MB written
+    # gemv_mma_kernel, Q6_K 128256x4096, N=8: 449.61 MB read + 5.48 MB written
     # (profiles/gemv_mma_q6_k_lmhead_n8.md)
-    "lmhead": ("74c65aef18225508", 455.21e6),
+    "lmhead": ("4262b8bab6772fc4", 455.09e6),
 }
 
 
@@ -184,8 +185,9 @@ def run_gpu(args):
     l2 = getattr(props, "L2_cache_size", 126 * 1024 * 1024) or 126 * 1024 * 1024
     R = args.copies
 
-    only = set(args.only.split(",")) if args.only else {"decode", "lmhead", "prefill"}
-    bad = only - {"decode", "lmhead", "prefill"}
+    all_ops = {"decode", "lmhead", "prefill", "prefill_f32"}
+    only = set(args.only.split(",")) if args.only else all_ops
+    bad = only - all_ops
     if bad:
         raise SystemExit(f"unknown op(s) in --only: {sorted(bad)}")
 
@@ -220,18 +222,28 @@ def run_gpu(args):
         def op_lmhead(r):
             chk(qmm.qmm_matmul(synth.Q6_K, head_w, Mh, Kh, head_x, Nh, head_y, stream=stream))
         ops["lmhead"], launches_per_pass["lmhead"] = op_lmhead, 1
-    if "prefill" in only:
+    if "prefill" in only or "prefill_f32" in only:
         pre_w = [make(synth.Q4_K, M, K, f"bench-prefill-{M}x{K}") for (M, K) in PREFILL_SHAPES]
         pre_x = [torch.from_numpy(synth.gen_x(PREFILL_N, K, f"bench-prefill-{K}")).to(dev)
                  for (_, K) in PREFILL_SHAPES]
         pre_y = [torch.empty(PREFILL_N, M, device=dev) for (M, _) in PREFILL_SHAPES]
-        pre_ws = [qmm.workspace_for(PREFILL_N, K, x) for x, (_, K) in zip(pre_x, PREFILL_SHAPES)]
+    if "prefill" in only:
+        # bf16 X: the GEMM alone (X in the tensor-core operand type)
+        pre_xb = [torch.from_numpy(synth.f32_to_bf16_bits(x.cpu().numpy())).to(dev).view(torch.bfloat16)
+                  for x in pre_x]
 
         def op_prefill(r):
             for i, (M, K) in enumerate(PREFILL_SHAPES):
+                chk(qmm.qmm_matmul(synth.Q4_K, pre_w[i][r], M, K, pre_xb[i], PREFILL_N, pre_y[i], stream=stream))
+        ops["prefill"], launches_per_pass["prefill"] = op_prefill, len(PREFILL_SHAPES)
+    if "prefill_f32" in only:
+        pre_ws = [qmm.workspace_for(PREFILL_N, K, x) for x, (_, K) in zip(pre_x, PREFILL_SHAPES)]
+
+        def op_prefill_f32(r):
+            for i, (M, K) in enumerate(PREFILL_SHAPES):
                 chk(qmm.qmm_matmul(synth.Q4_K, pre_w[i][r], M, K, pre_x[i], PREFILL_N, pre_y[i], pre_ws[i],
                                    stream=stream))
-        ops["prefill"], launches_per_pass["prefill"] = op_prefill, 2 * len(PREFILL_SHAPES)
+        ops["prefill_f32"], launches_per_pass["prefill_f32"] = op_prefill_f32, 2 * len(PREFILL_SHAPES)
     rot_bytes = R * sum(wbytes(synth.Q4_0, M, K) for M, K in DECODE_SHAPES)
     torch.cuda.synchronize()
 
@@ -305,14 +317,17 @@ def run_gpu(args):
     decode_gbs = dec_bytes / (med["decode"] * 1e-3) / 1e9 * world if "decode" in med else None
     head_gbs = head_bytes / (med["lmhead"] * 1e-3) / 1e9 * world if "lmhead" in med else None
     pre_tflops = pre_flops / (med["prefill"] * 1e-3) / 1e12 * world if "prefill" in med else None
+    pre32_tflops = pre_flops / (med["prefill_f32"] * 1e-3) / 1e12 * world if "prefill_f32" in med else None
 
     # dominant kernel of the step -> roofline object
     shares = {k: v / sum(med.values()) for k, v in med.items()}
     dom = max(shares, key=shares.get)
-    if dom == "prefill":
-        roof = {"bound": "tensor", "achieved": round(pre_tflops, 1), "peak": bf16_peak, "unit": "TFLOP/s",
-                "frac": round(pre_tflops / bf16_peak, 4), "traffic": traffic_for("prefill"),
-                "kernel": "gemm_tc (Q4_K, N=512) + x_to_bf16", "peak_source": f"bf16_tflops ({peak_src})"}
+    if dom in ("prefill", "prefill_f32"):
+        tf = pre_tflops if dom == "prefill" else pre32_tflops
+        roof = {"bound": "tensor", "achieved": round(tf, 1), "peak": bf16_peak, "unit": "TFLOP/s",
+                "frac": round(tf / bf16_peak, 4), "traffic": traffic_for(dom),
+                "kernel": "gemm_tc (Q4_K, N=512)" + ("" if dom == "prefill" else " + x_to_bf16"),
+                "peak_source": f"bf16_tflops ({peak_src})"}
     elif dom == "lmhead":
         roof = {"bound": "hbm", "achieved": round(head_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
                 "frac": round(head_gbs / hbm_peak, 4), "traffic": traffic_for("lmhead"),
@@ -390,8 +405,12 @@ def run_gpu(args):
                           "us": round(med["lmhead"] * 1e3, 3), "N": Nh}
     if pre_tflops is not None:
         line["prefill"] = {"TFLOPs": r1(pre_tflops), "frac_of_measured_bf16": round(pre_tflops / bf16_peak, 4),
-                           "us": round(med["prefill"] * 1e3, 3), "N": PREFILL_N,
-                           "includes": "f32->bf16 conversion of X + tensor-core GEMM"}
+                           "us": round(med["prefill"] * 1e3, 3), "N": PREFILL_N, "x": "bf16",
+                           "includes": "tensor-core GEMM"}
+    if pre32_tflops is not None:
+        line["prefill_f32"] = {"TFLOPs": r1(pre32_tflops), "frac_of_measured_bf16": round(pre32_tflops / bf16_peak, 4),
+                               "us": round(med["prefill_f32"] * 1e3, 3), "N": PREFILL_N, "x": "f32",
+                               "includes": "f32->bf16 conversion of X + tensor-core GEMM"}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     if rank == 0:
@@ -479,7 +498,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-static-weights", action="store_true",
                     help="launch every call only after the preceding kernel has finished")
-    ap.add_argument("--only", default="", help="comma list of ops to run (decode,lmhead,prefill); default all")
+    ap.add_argument("--only", default="",
+                    help="comma list of ops to run (decode,lmhead,prefill,prefill_f32); default all")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
