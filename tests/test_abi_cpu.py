@@ -9,7 +9,8 @@ import re
 
 import pytest
 
-from block_quantized_gemv_gguf_gb300 import build, qmm
+import oracle
+from block_quantized_gemv_gguf_gb300 import build, qmm, synth
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -46,7 +47,11 @@ def test_block_info(lib):
     assert qmm.qmm_block_info(qmm.Q4_0) == (0, 32, 18)
     assert qmm.qmm_block_info(qmm.Q4_K) == (0, 256, 144)
     assert qmm.qmm_block_info(qmm.Q6_K) == (0, 256, 210)
+    assert qmm.qmm_block_info(qmm.Q5_K) == (0, 256, 176)
     assert qmm.qmm_block_info(9)[0] == qmm.ERR_INVALID_ARG
+    # the library, the oracle and the input generators agree on every format
+    for wt, (e, b) in synth.BLOCK.items():
+        assert qmm.qmm_block_info(wt) == (0, e, b) and oracle.block_info(wt) == (e, b)
 
 
 def test_status_strings(lib):
