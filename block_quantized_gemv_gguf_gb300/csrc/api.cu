@@ -120,7 +120,6 @@ struct Settings {
     int gemv_max_n;   // QMM_GEMV_MAX_N: largest N qmm_matmul sends to the GEMV
     int force;        // QMM_FORCE_PATH: 0 none, 1 gemv, 2 gemm
     int gemm_bn;      // QMM_GEMM_BN: 0 = model-based choice
-    int gemm_cl;      // QMM_GEMM_CL: CTAs per cluster sharing X tiles (1, 2, 4); 0 = default
     int gemv_rows;    // QMM_GEMV_ROWS: 64, 128 or 256 rows per GEMV tile; 0 = by M
     int gemv_rg;      // QMM_GEMV_RG: 16-row groups per warp (1 or 2) of the resident-X GEMV
     int gemv_ks;      // QMM_GEMV_KS: K split of the GEMV (1..8); 0 = automatic
@@ -136,8 +135,6 @@ const Settings &settings() {
         t.force = (f && !std::strcmp(f, "gemv")) ? 1 : (f && !std::strcmp(f, "gemm")) ? 2 : 0;
         t.gemm_bn = env_int("QMM_GEMM_BN", 0);
         if (t.gemm_bn != 64 && t.gemm_bn != 128 && t.gemm_bn != 256) t.gemm_bn = 0;
-        t.gemm_cl = env_int("QMM_GEMM_CL", 0);
-        if (t.gemm_cl != 1 && t.gemm_cl != 2 && t.gemm_cl != 4) t.gemm_cl = 0;
         t.gemv_rows = env_int("QMM_GEMV_ROWS", 0);
         if (t.gemv_rows != 64 && t.gemv_rows != 128 && t.gemv_rows != 256) t.gemv_rows = 0;
         t.gemv_rg = env_int("QMM_GEMV_RG", 0) == 2 ? 2 : 1;
@@ -395,7 +392,6 @@ qmm_status gemm_impl(int wt, const void *W, size_t w_bytes, int64_t M, int64_t K
     a.K = K;
     a.N = (int)N;
     a.bn = bn;
-    a.cl = settings().gemm_cl ? settings().gemm_cl : 1;
     a.Y = Y;
     a.status = di.status;
     a.wait_limit = g_wait_limit.load();

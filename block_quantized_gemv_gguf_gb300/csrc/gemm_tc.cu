@@ -16,8 +16,6 @@
 //               hides behind the other warps); afterwards the same warps
 //               read the accumulator out of TMEM (two warps per lane
 //               quarter, half of the columns each) and store Y.
-// Optionally (CL > 1) the CTAs of a cluster along M share each X tile through
-// TMA multicast from cluster rank 0.
 // Each weight block is dequantized once per CTA and reused by all BN token
 // columns of the MMA, which is what makes the tile compute-bound at N >= 256
 // ("cera 0.3.1 src/model/gpu_lfm2.rs", build_mul_mat_pipeline: decode a
@@ -72,8 +70,8 @@ template <int F, int BN> struct Layout {
     static constexpr int OFF_X = 0;
     static constexpr int OFF_RAW = OFF_X + SX * XSLOT;
     static constexpr int OFF_BAR = OFF_RAW + SR * RAW_BYTES;
-    // raw_full/empty[SR], x_full/empty/cempty[SX], a_full/empty[SA], acc_full
-    static constexpr int NUM_BARS = 2 * SR + 3 * SX + 2 * SA + 1;
+    // raw_full/empty[SR], x_full/empty[SX], a_full/empty[SA], acc_full
+    static constexpr int NUM_BARS = 2 * SR + 2 * SX + 2 * SA + 1;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int TOTAL = OFF_MISC + 64;
     static constexpr int SMEM = TOTAL + 1024;     // 1024-byte alignment slack
@@ -233,7 +231,7 @@ __device__ __forceinline__ void dequant32<Q6_K>(const uint8_t *rb, int sub, int 
     }
 }
 
-template <int F, int BN, int CL>
+template <int F, int BN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap, int M, int K,
                    int N, float *__restrict__ Y, unsigned *status, uint64_t wait_limit) {
@@ -250,13 +248,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     constexpr int SR = L::SR;
     uint64_t *raw_full = bars, *raw_empty = bars + SR;
     uint64_t *x_full = bars + 2 * SR, *x_empty = x_full + SX;
-    uint64_t *x_cempty = x_empty + SX;       // leader only: slot free and armed in all CL CTAs
-    uint64_t *a_full = x_cempty + SX, *ab_empty = a_full + SA;   // ab_empty: A slot consumed by the MMA
+    uint64_t *a_full = x_empty + SX, *ab_empty = a_full + SA;   // ab_empty: A slot consumed by the MMA
     uint64_t *acc_full = ab_empty + SA;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
     unsigned *abort_flag = reinterpret_cast<unsigned *>(smem + L::OFF_MISC + 4);
-    unsigned *x_issued = reinterpret_cast<unsigned *>(smem + L::OFF_MISC + 8);    // copies the leader issued
-    unsigned *x_seen = reinterpret_cast<unsigned *>(smem + L::OFF_MISC + 12);     // X tiles the MMA consumed
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.x * BM, n0 = blockIdx.y * BN;
@@ -265,8 +260,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // Each CTA walks K starting at its own chunk (a rotation): CTAs that run
     // in lockstep then read different X tiles at any moment instead of all
     // hitting the same L2 lines at once.  The k-sum is the same set of terms.
-    // (the CTAs of a cluster share X tiles, so they share the rotation)
-    const int koff = (int)(((blockIdx.x / (unsigned)CL) * 5u + blockIdx.y * 3u) % (unsigned)nkc);
+    const int koff = (int)((blockIdx.x * 5u + blockIdx.y * 3u) % (unsigned)nkc);
     auto kchunk = [&](int c) { return c + koff < nkc ? c + koff : c + koff - nkc; };
     const Ctl ctl{abort_flag, wait_limit};
     const uint64_t drain_limit = wait_limit < (1ull << 31) ? (1ull << 31) : wait_limit;
@@ -279,7 +273,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int s = 0; s < SX; ++s) {
             mbar_init(&x_full[s], 1);
             mbar_init(&x_empty[s], 1);
-            mbar_init(&x_cempty[s], CL);
         }
         for (int s = 0; s < SA; ++s) {
             mbar_init(&a_full[s], DQW);
@@ -287,8 +280,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         mbar_init(acc_full, 1);
         *abort_flag = 0u;
-        *x_issued = 0u;
-        *x_seen = 0u;
         fence_barrier_init();
     }
     if (warp == WARP_WPROD && lane == 0) prefetch_tensormap(&wmap);
@@ -298,14 +289,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tmem_relinquish();
     }
     tc_fence_before();
-    if constexpr (CL > 1)
-        cluster_sync_all();   // barriers of every CTA initialized before any remote arrive or multicast
-    else
-        __syncthreads();
+    __syncthreads();
     tc_fence_after();
     const uint32_t tmem_d = *tmem_slot;
     pdl_launch_dependents();
-    const uint32_t crank = CL > 1 ? cluster_ctarank() : 0u;
 
     if (warp == WARP_WPROD) {
         if (lane == 0) {
@@ -339,7 +326,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // preceding kernel, e.g. the bf16 conversion) only after it ends.
             pdl_wait();
             int issued = 0;   // X copies (rounds of XG stages) this lane issued: rounds lane + XL*i, i < issued
-            const uint32_t leader_cempty = CL > 1 ? cluster_addr(x_cempty, 0u) : 0u;
             constexpr int XG = L::XG;
             const int nrounds = nsteps / XG;
             for (int u = lane; u < nrounds; u += XL) {
@@ -349,20 +335,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 mbar_arrive_expect_tx(&x_full[s], (uint32_t)L::XSLOT);   // this CTA's slot s: armed
                 const int t0 = u * XG;                                    // first stage of the round
                 const int kb = kchunk(t0 / (KC / BK)) * (KC / BK) + t0 % (KC / BK);   // its 64-k block
-                if constexpr (CL == 1) {
-                    tma_load_3d(sX + s * L::XSLOT, &xmap, &x_full[s], 0, n0, kb);
-                    ++issued;
-                } else {
-                    mbar_arrive_remote(leader_cempty + 8u * (uint32_t)s);
-                    if (crank == 0) {
-                        if (!wait_ok(ctl, &x_cempty[s], (u / SX) & 1, wait_limit)) break;
-                        tma_load_3d_mc(sX + s * L::XSLOT, &xmap, &x_full[s], 0, n0, kb, (uint16_t)((1u << CL) - 1u));
-                        ++issued;
-                    }
-                }
+                tma_load_3d(sX + s * L::XSLOT, &xmap, &x_full[s], 0, n0, kb);
+                ++issued;
             }
-            if (CL > 1 && crank == 0) *x_issued = (unsigned)issued;
-            if (CL == 1 && *abort_flag)   // drain this lane's copies that may still be in flight
+            if (*abort_flag)   // drain this lane's copies that may still be in flight
                 for (int i = 0; i < issued; ++i) {
                     const int u = lane + XL * i;
                     if (u + SX >= lane + XL * issued) drain(&x_full[u % SX], (u / SX) & 1, drain_limit);
@@ -374,10 +350,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             constexpr int XG = L::XG;
             for (int t = 0; t < nsteps; ++t) {
                 const int u = t / XG, j = t % XG, sx = u % SX, sa = t % SA;
-                if (j == 0) {
-                    if (!wait_ok(ctl, &x_full[sx], (u / SX) & 1, wait_limit)) break;
-                    *x_seen = (unsigned)(u + 1);
-                }
+                if (j == 0 && !wait_ok(ctl, &x_full[sx], (u / SX) & 1, wait_limit)) break;
                 if (!wait_ok(ctl, &a_full[sa], (t / SA) & 1, wait_limit)) break;
                 tc_fence_after();
                 const uint32_t a0 = tmem_d + (uint32_t)(L::A_COL0 + 32 * sa);   // lane 0, first column
@@ -466,17 +439,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     tc_fence_before();
     __syncthreads();
-    if constexpr (CL > 1) {
-        // No CTA may exit while a multicast copy into it is in flight.  The
-        // leader publishes how many copies it issued; after the cluster
-        // barrier every CTA waits (bounded) for those it has not consumed.
-        if (crank == 0 && threadIdx.x == 0)
-            for (uint32_t r = 1; r < (uint32_t)CL; ++r) st_cluster_u32(cluster_addr(x_issued, r), *x_issued);
-        cluster_sync_all();
-        if (warp == WARP_XPROD && lane == 0)
-            for (unsigned u = *x_seen; u < *x_issued; ++u)
-                drain(&x_full[u % SX], (u / SX) & 1, drain_limit);
-    }
     if (warp == WARP_MMA) {
         tc_fence_after();
         tmem_dealloc(tmem_d, L::TMEM_COLS);
@@ -484,10 +446,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (threadIdx.x == 0 && *abort_flag) report_status(status, kStatusTimeout);
 }
 
-template <int F, int BN, int CL>
+template <int F, int BN>
 cudaError_t launch_one(const GemmArgs &a, const CUtensorMap &wmap, const CUtensorMap &xmap, cudaStream_t st) {
     using L = Layout<F, BN>;
-    auto kern = gemm_tc_kernel<F, BN, CL>;
+    auto kern = gemm_tc_kernel<F, BN>;
     static std::atomic<uint64_t> configured{0};   // one bit per device ordinal
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -500,19 +462,12 @@ cudaError_t launch_one(const GemmArgs &a, const CUtensorMap &wmap, const CUtenso
     }
     cudaLaunchConfig_t cfg = {};
     const int64_t tiles_m = (a.M + BM - 1) / BM;
-    cfg.gridDim = dim3((unsigned)((tiles_m + CL - 1) / CL * CL), (unsigned)((a.N + BN - 1) / BN), 1);
+    cfg.gridDim = dim3((unsigned)tiles_m, (unsigned)((a.N + BN - 1) / BN), 1);
     cfg.blockDim = dim3(NUM_THREADS, 1, 1);
     cfg.dynamicSmemBytes = L::SMEM;
     cfg.stream = st;
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[1];
     unsigned na = 0;
-    if (CL > 1) {
-        attr[na].id = cudaLaunchAttributeClusterDimension;
-        attr[na].val.clusterDim.x = CL;
-        attr[na].val.clusterDim.y = 1;
-        attr[na].val.clusterDim.z = 1;
-        ++na;
-    }
     if (a.pdl) {
         attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[na].val.programmaticStreamSerializationAllowed = 1;
@@ -525,22 +480,12 @@ cudaError_t launch_one(const GemmArgs &a, const CUtensorMap &wmap, const CUtenso
     return cudaGetLastError();
 }
 
-template <int F, int BN>
-cudaError_t launch_cl(const GemmArgs &a, const CUtensorMap &wmap, const CUtensorMap &xmap, cudaStream_t st) {
-    switch (a.cl) {
-    case 1: return launch_one<F, BN, 1>(a, wmap, xmap, st);
-    case 2: return launch_one<F, BN, 2>(a, wmap, xmap, st);
-    case 4: return launch_one<F, BN, 4>(a, wmap, xmap, st);
-    default: return cudaErrorInvalidValue;
-    }
-}
-
 template <int F>
 cudaError_t launch_fmt(const GemmArgs &a, const CUtensorMap &wmap, const CUtensorMap &xmap, cudaStream_t st) {
     switch (a.bn) {
-    case 64: return launch_cl<F, 64>(a, wmap, xmap, st);
-    case 128: return launch_cl<F, 128>(a, wmap, xmap, st);
-    case 256: return launch_cl<F, 256>(a, wmap, xmap, st);
+    case 64: return launch_one<F, 64>(a, wmap, xmap, st);
+    case 128: return launch_one<F, 128>(a, wmap, xmap, st);
+    case 256: return launch_one<F, 256>(a, wmap, xmap, st);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -108,7 +108,6 @@ struct GemmArgs {
     int64_t M, K;
     int N;
     int bn;          // token tile (64, 128 or 256)
-    int cl;          // CTAs per cluster sharing each X tile by multicast (1, 2 or 4)
     float *Y;
     unsigned *status;
     uint64_t wait_limit;

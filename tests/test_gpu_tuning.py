@@ -97,17 +97,16 @@ print("BAD" if bad else "OK", bad)
 '''
 
 GEMM_COMBOS = [
-    {"QMM_GEMM_CL": "1", "QMM_GEMM_BN": "256"},
-    {"QMM_GEMM_CL": "2", "QMM_GEMM_BN": "64"},
-    {"QMM_GEMM_CL": "4", "QMM_GEMM_BN": "128"},
-    {"QMM_GEMM_CL": "4", "QMM_GEMM_BN": "256"},
+    {"QMM_GEMM_BN": "64"},
+    {"QMM_GEMM_BN": "128"},
+    {"QMM_GEMM_BN": "256"},
 ]
 
 
 @pytest.mark.parametrize("env", GEMM_COMBOS, ids=lambda e: "-".join(f"{k[9:].lower()}{v}" for k, v in e.items()))
 def test_forced_gemm_shapes(env):
-    """The tensor-core GEMM with every cluster size and token tile (M not a
-    multiple of the cluster's rows: the padding CTAs must stay silent)."""
+    """The tensor-core GEMM with every token tile (M not a multiple of the
+    128-row tile: the partial tiles must stay inside Y)."""
     import torch
     if not torch.cuda.is_available():
         pytest.skip("needs a GPU")
