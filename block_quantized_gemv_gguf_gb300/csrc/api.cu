@@ -124,6 +124,11 @@ struct Settings {
     int gemv_rg;      // QMM_GEMV_RG: 16-row groups per warp (1 or 2) of the resident-X GEMV
     int gemv_ks;      // QMM_GEMV_KS: K split of the GEMV (1..8); 0 = automatic
     int gemv_res;     // QMM_GEMV_RESIDENT: 0 disables the resident-X GEMV
+    int stream;       // QMM_GEMV_STREAM: 0 disables the streaming N = 1 GEMV
+    int stream_warps; // QMM_STREAM_WARPS: warps per CTA of the streaming GEMV (0 = by shared memory)
+    int tc;           // QMM_GEMV_TC: 0 disables the 16-row-tile tensor-core GEMV (N <= 8)
+    int tc_warps;     // QMM_TC_WARPS: warps per CTA of that kernel (0 = by shared memory)
+    int tc_max_n;     // QMM_TC_MAX_N: largest N it serves (default 4; above, the ring GEMV is faster)
 };
 const Settings &settings() {
     static Settings s = [] {
@@ -141,6 +146,16 @@ const Settings &settings() {
         t.gemv_ks = env_int("QMM_GEMV_KS", 0);
         if (t.gemv_ks < 0 || t.gemv_ks > 8) t.gemv_ks = 0;
         t.gemv_res = env_int("QMM_GEMV_RESIDENT", 1) != 0;
+        t.stream = env_int("QMM_GEMV_STREAM", 1) != 0;
+        t.stream_warps = env_int("QMM_STREAM_WARPS", 0);
+        if (t.stream_warps != 4 && t.stream_warps != 8 && t.stream_warps != 12 && t.stream_warps != 16)
+            t.stream_warps = 0;
+        t.tc = env_int("QMM_GEMV_TC", 1) != 0;
+        t.tc_warps = env_int("QMM_TC_WARPS", 0);
+        if (t.tc_warps != 4 && t.tc_warps != 8 && t.tc_warps != 16) t.tc_warps = 0;
+        t.tc_max_n = env_int("QMM_TC_MAX_N", 4);
+        if (t.tc_max_n < 1) t.tc_max_n = 1;
+        if (t.tc_max_n > 8) t.tc_max_n = 8;
         return t;
     }();
     return s;
@@ -260,6 +275,34 @@ qmm_status gemv_segments(int wt, const SegIn *seg, int nseg, int64_t K, const vo
     bool fast = K % 256 == 0 && row_bytes % 16 == 0 && (uintptr_t)X % 16 == 0 && m_total <= (1ll << 31) - 1;
     for (int i = 0; i < nseg; ++i) fast = fast && (uintptr_t)seg[i].W % 16 == 0;
     if (q8) fast = fast && (uintptr_t)xscales % 16 == 0;
+    if (fast && nseg == 1 && N == 1 && !amax && !q8 && settings().stream) {
+        // one token: the streaming kernel, when the shape fits it
+        StreamPlan sp{};
+        if (plan_gemv_stream(wt, seg[0].M, K, di.num_sms, settings().stream_warps, sp))
+            return from_cuda(launch_gemv_stream(wt, sp, static_cast<const uint8_t *>(seg[0].W), seg[0].M, K, X,
+                                                xt == QMM_X_BF16, seg[0].Y, static_weights(), di.status,
+                                                g_wait_limit.load(), st));
+    }
+    if (fast && nseg == 1 && N >= 2 && N <= settings().tc_max_n && !amax && !q8 && settings().tc && gemv_tc_unit_bytes(wt)) {
+        // several tokens: 16-row tiles on the tensor cores, when the shape fits
+        TcPlan tp{};
+        if (plan_gemv_tc(wt, seg[0].M, K, (int)N, di.num_sms, settings().tc_warps, tp)) {
+            EncodeTiledFn enc = encode_fn();
+            if (!enc) return QMM_ERR_CUDA;
+            CUtensorMap wmap;
+            cuuint64_t dims[2] = {(cuuint64_t)(row_bytes / 2), (cuuint64_t)seg[0].M};
+            cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+            cuuint32_t box[2] = {(cuuint32_t)(gemv_tc_unit_bytes(wt) / 2), 16u};
+            cuuint32_t estr[2] = {1u, 1u};
+            if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void *>(seg[0].W), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                return QMM_ERR_CUDA;
+            return from_cuda(launch_gemv_tc(wt, tp, wmap, static_cast<const uint8_t *>(seg[0].W), seg[0].M, K, X,
+                                            xt == QMM_X_BF16, (int)N, seg[0].Y, static_weights(), di.status,
+                                            g_wait_limit.load(), st));
+        }
+    }
     if (fast) {
         EncodeTiledFn enc = encode_fn();
         if (!enc) return QMM_ERR_CUDA;

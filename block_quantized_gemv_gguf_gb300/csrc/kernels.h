@@ -58,6 +58,39 @@ cudaError_t launch_gemv_mma(int fmt, const GemvPlan &plan, const GemvSegs &segs,
                             cudaStream_t st, unsigned long long *amax_ws = nullptr, int32_t *idx = nullptr,
                             float *val = nullptr);
 
+// Streaming decode GEMV for N = 1 (K % 256 == 0, K <= 32768, 16-byte
+// aligned W, rows and X): one CTA of `warps` warps per SM owns whole rows,
+// each warp streams 32-unit stages of them through S shared-memory slots.
+struct StreamPlan {
+    int grid;
+    int warps;
+    int S;
+    int smem;   // dynamic shared memory bytes
+};
+// false: the shape does not fit the kernel (another GEMV kernel runs).
+// force_warps > 0 requests that many warps per CTA.
+bool plan_gemv_stream(int fmt, int64_t M, int64_t K, int num_sms, int force_warps, StreamPlan &p);
+// y[M] = W x.  pdl: programmatic dependent of the preceding kernel (the
+// weight copies start before it ends; X and Y wait for it).
+cudaError_t launch_gemv_stream(int fmt, const StreamPlan &p, const uint8_t *W, int64_t M, int64_t K, const void *X,
+                               int xbf16, float *Y, bool pdl, unsigned *status, uint64_t limit, cudaStream_t st);
+
+// Tensor-core GEMV for 1 <= N <= 8 (mma.sync f16 on the exact codes) of
+// Q8_0 / Q4_0 / Q4_K / Q5_K rows (K % 256 == 0, K <= 32768, 16-byte aligned
+// W, rows and X).  wmap: W as u16 [M][row_bytes / 2], box
+// {gemv_tc_unit_bytes / 2, 16}.  One CTA per SM owns whole 16-row groups.
+struct TcPlan {
+    int grid;
+    int warps;
+    int S;
+    int smem;
+};
+int gemv_tc_unit_bytes(int fmt);   // 0: format not handled
+bool plan_gemv_tc(int fmt, int64_t M, int64_t K, int N, int num_sms, int force_warps, TcPlan &p);
+cudaError_t launch_gemv_tc(int fmt, const TcPlan &p, const CUtensorMap &wmap, const uint8_t *W, int64_t M, int64_t K,
+                           const void *X, int xbf16, int N, float *Y, bool pdl, unsigned *status, uint64_t limit,
+                           cudaStream_t st);
+
 // Integer tensor-core GEMV (mma.sync m16n8k32 on the weights' integer codes),
 // same weight maps, segments, plans and argmax mode as launch_gemv_mma.
 //  * exact: X f32 or bf16 [N][K] as exact int8 digits; N <= 2 (Q6_K: N == 1).
