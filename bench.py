@@ -1,18 +1,32 @@
 #!/usr/bin/env python3
-"""Benchmark of the block-quantized projection matmul on one GB300.
+"""Benchmark of the block-quantized projection matmul on GB300.
 
-Headline workload: the Q4_0 decode GEMV at N=1 on the Llama-3-8B projection
-shapes (M,K) = (4096,4096), (1024,4096), (14336,4096), (4096,14336); `value`
-is its effective HBM bandwidth (algorithmic bytes / device time, GB/s).
-One step runs the whole hot path once over one batch of synthetic input:
-  decode   4 x Q4_0 GEMV, N=1                          (decode GEMV)
-  lmhead   Q6_K 128256 x 4096 LM head, N=8, f32 X     (small-N GEMV)
-  prefill      Q4_K 4096x4096 and 14336x4096, N=512, bf16 X (tcgen05 GEMM)
-  prefill_f32  the same with f32 X (x->bf16 conversion + tcgen05 GEMM)
-Weights are replicated into R device copies whose total size exceeds L2
-several times, and step s uses copy s % R (rotating inputs > L2 instead of an
-L2 flush).  Each op is captured in a CUDA graph over all R copies and timed
-with CUDA events on the launching stream; the step time is the sum.
+Headline: the Q4_0 decode GEMV at N=1 on the Llama-3-8B projection shapes
+(M,K) = (4096,4096), (1024,4096), (14336,4096), (4096,14336); `value` is its
+effective HBM bandwidth (algorithmic bytes / device time, GB/s).
+
+One timed step runs the whole hot path once over one batch of synthetic input:
+  decode       4 x Q4_0 GEMV, N=1 (one CUDA graph per shape)   decode GEMV
+  lmhead       Q6_K 128256 x 4096 LM head, N=8, f32 X          small-N GEMV
+  prefill      Q4_K 4096x4096 and 14336x4096, N=512, bf16 X    tcgen05 GEMM
+  prefill_f32  the same with f32 X (x -> bf16 + GEMM)
+Weights are replicated into R device copies whose total exceeds L2, and
+step s uses copy s % R (inputs larger than L2 instead of a flush).  Each op is
+a CUDA graph over all R copies, timed with CUDA events on the launching
+stream.
+
+After the timed steps (outside the step time) the other workloads are timed
+the same way and reported under "workloads": the Q8_0 256x512 GEMV, the
+Q4_K prefill at N = 64 and 256, the LM head at N = 1 and 4, and the 32-layer
+decoder sweep (224 projections, one graph per N, tokens/s).  Every op's
+output is then checked on sampled rows against the oracle.
+
+Multi-GPU (torchrun, one rank per GPU, NCCL): each rank owns a row slice of
+every weight matrix (the LM head: a vocabulary slice), X is replicated, no
+collective runs on the data path unless --allgather asks for Y to be
+gathered.  --scaling weak (default): per-GPU rows fixed at the single-GPU
+shapes (the global matrices have G x M rows); --scaling strong: the global
+shapes are the single-GPU ones, split G ways.
 
 --impl reference runs the oracle (plain C, f64, host cores) on a bounded
 sample of the same workload and prints the same JSON line with
@@ -35,6 +49,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from block_quantized_gemv_gguf_gb300 import synth  # noqa: E402
+from block_quantized_gemv_gguf_gb300.shard import row_partition  # noqa: E402
 
 DECODE_SHAPES = [(4096, 4096), (1024, 4096), (14336, 4096), (4096, 14336)]
 LMHEAD = (128256, 4096, 8)
@@ -45,6 +60,7 @@ WORKLOAD = ("Q4_0 decode GEMV N=1 on Llama-3-8B projection shapes (4096,4096) (1
             "(4096,14336); same step also runs the Q6_K 128256x4096 LM head at N=8 and the Q4_K "
             "(4096,4096)+(14336,4096) prefill GEMM at N=512 with bf16 X and with f32 X")
 NOMINAL_HBM_GBS = 8000.0
+ALL_OPS = ("decode", "lmhead", "prefill", "prefill_f32")
 
 
 def peaks():
@@ -55,15 +71,11 @@ def peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
-# DRAM bytes (read + write) per pass of an op, summed over its kernels, from
-# one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum), keyed by the
-# sha256 of the kernel sources they were taken on.  A source change since the
-# capture turns the figure into null.
-TRAFFIC = {
-    # gemv_mma_kernel, Q6_K 128256x4096, N=8: 449.53 MB read + 5.59 MB written
-    # (profiles/gemv_mma_q6_k_lmhead_n8.md)
-    "lmhead": ("fd99067e98516dce", 455.11e6),
-}
+# DRAM bytes (read + write) per launch of the dominant kernels, from one ncu
+# capture each (dram__bytes_read.sum + dram__bytes_write.sum), keyed by the
+# sha256 of the kernel sources they were taken on: any source change since
+# the capture turns the figure into null.
+TRAFFIC = {}
 
 
 def _kernel_hash():
@@ -88,6 +100,7 @@ def wbytes(wt, M, K):
 
 
 def alg_bytes(wt, M, K, N, xs):
+    """Algorithmic bytes of one call: weights + X + Y."""
     return wbytes(wt, M, K) + N * K * xs + N * M * 4
 
 
@@ -145,8 +158,7 @@ class Clocks:
 
 
 # ---------------------------------------------------------------------------
-# multi-rank aggregation (each rank runs the whole step on its own GPU: weak
-# scaling, no data-path collective)
+# multi-rank helpers
 # ---------------------------------------------------------------------------
 def max_over_ranks(values: dict, world: int, device) -> dict:
     """Per-op times (ms per step), maximum over all ranks; unchanged when
@@ -161,9 +173,46 @@ def max_over_ranks(values: dict, world: int, device) -> dict:
     return {k: float(v) for k, v in zip(keys, t.tolist())}
 
 
+def local_rows(M, world, rank, scaling, align=16):
+    """(r0, r1) of the global matrix this rank owns, and the global M."""
+    if world <= 1:
+        return 0, M, M
+    if scaling == "weak":
+        Mg = M * world
+        return rank * M, (rank + 1) * M, Mg
+    r0, r1 = row_partition(M, world, rank, align)
+    return r0, r1, M
+
+
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
+class Timer:
+    """CUDA graph of `passes` passes of f over rotating inputs; replays timed
+    with CUDA events on the launching stream."""
+
+    def __init__(self, torch, stream, f, passes):
+        self.torch, self.stream, self.passes = torch, stream, passes
+        self.g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.g, stream=stream):
+            for r in range(passes):
+                f(r)
+
+    def replay(self):
+        t = self.torch
+        a, b = t.cuda.Event(enable_timing=True), t.cuda.Event(enable_timing=True)
+        with t.cuda.stream(self.stream):
+            a.record(self.stream)
+            self.g.replay()
+            b.record(self.stream)
+        return a, b
+
+    def median_ms(self, reps):
+        evs = [self.replay() for _ in range(reps)]
+        self.torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) for a, b in evs) / self.passes
+
+
 def run_gpu(args):
     import torch
     from block_quantized_gemv_gguf_gb300 import qmm
@@ -184,67 +233,95 @@ def run_gpu(args):
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 126 * 1024 * 1024) or 126 * 1024 * 1024
     R = args.copies
+    stream = torch.cuda.Stream(device=dev)
 
-    all_ops = {"decode", "lmhead", "prefill", "prefill_f32"}
-    only = set(args.only.split(",")) if args.only else all_ops
-    bad = only - all_ops
+    only = set(args.only.split(",")) if args.only else set(ALL_OPS)
+    bad = only - set(ALL_OPS)
     if bad:
         raise SystemExit(f"unknown op(s) in --only: {sorted(bad)}")
-
-    # ---- inputs: generated once on the host, replicated R times on device ----
-    def make(wt, M, K, name):
-        w = torch.from_numpy(synth.gen_weights(wt, M, K, name)).to(dev)
-        return [w] + [w.clone() for _ in range(R - 1)]
-
-    stream = torch.cuda.Stream(device=dev)
 
     def chk(s):
         if s != qmm.OK:
             raise RuntimeError(qmm.status_name(s))
 
-    ops, launches_per_pass = {}, {}
+    def gen_rows(wt, M, K, name, r0, r1, Mg):
+        """Rows [r0, r1) of the global matrix (Mg rows) `name`, host bytes.
+        Weak scaling: each rank's slice is its own seeded draw (the global
+        matrix is the concatenation); strong: a slice of the single-GPU matrix."""
+        if Mg == M and r0 == 0 and r1 == M:
+            return synth.gen_weights(wt, M, K, name)
+        if args.scaling == "weak":
+            return synth.gen_weights(wt, r1 - r0, K, f"{name}/rows{r0}-{r1}")
+        full = synth.gen_weights(wt, Mg, K, name)
+        rb = synth.row_bytes(wt, K)
+        return full[r0 * rb:r1 * rb].copy()
+
+    def copies(w):
+        t = torch.from_numpy(w).to(dev)
+        return [t] + [t.clone() for _ in range(R - 1)]
+
+    # ---- inputs of the timed step (this rank's rows) ----
+    ops, launches_per_pass, host = {}, {}, {}
     Mh, Kh, Nh = LMHEAD
     if "decode" in only:
-        dec_w = [make(synth.Q4_0, M, K, f"bench-decode-{M}x{K}") for (M, K) in DECODE_SHAPES]
-        dec_x = [torch.from_numpy(synth.gen_x(1, K, f"bench-decode-{K}")).to(dev) for (_, K) in DECODE_SHAPES]
-        dec_y = [torch.empty(1, M, device=dev) for (M, _) in DECODE_SHAPES]
-
-        def op_decode(r):
-            for i, (M, K) in enumerate(DECODE_SHAPES):
-                chk(qmm.qmm_matmul(synth.Q4_0, dec_w[i][r], M, K, dec_x[i], 1, dec_y[i], stream=stream))
-        ops["decode"], launches_per_pass["decode"] = op_decode, len(DECODE_SHAPES)
+        dec = []
+        for (M, K) in DECODE_SHAPES:
+            r0, r1, Mg = local_rows(M, world, rank, args.scaling)
+            w = gen_rows(synth.Q4_0, M, K, f"bench-decode-{M}x{K}", r0, r1, Mg)
+            x = synth.gen_x(1, K, f"bench-decode-{K}")
+            dec.append(dict(M=r1 - r0, K=K, Mg=Mg, w=w, W=copies(w), x=x, X=torch.from_numpy(x).to(dev),
+                            Y=torch.empty(1, r1 - r0, device=dev)))
+        for i, d in enumerate(dec):
+            def op(r, d=d):
+                chk(qmm.qmm_matmul(synth.Q4_0, d["W"][r], d["M"], d["K"], d["X"], 1, d["Y"], stream=stream))
+            ops[f"decode{i}"], launches_per_pass[f"decode{i}"] = op, 1
+        host["decode"] = dec
     if "lmhead" in only:
-        # one copy: 431 MB alone is more than three times L2
-        head_w = torch.from_numpy(synth.gen_weights(synth.Q6_K, Mh, Kh, "bench-lmhead")).to(dev)
-        head_x = torch.from_numpy(synth.gen_x(Nh, Kh, "bench-lmhead")).to(dev)
-        head_y = torch.empty(Nh, Mh, device=dev)
+        r0, r1, Mg = local_rows(Mh, world, rank, args.scaling)
+        w = gen_rows(synth.Q6_K, Mh, Kh, "bench-lmhead", r0, r1, Mg)
+        x = synth.gen_x(Nh, Kh, "bench-lmhead")
+        hd = dict(M=r1 - r0, w=w, W=torch.from_numpy(w).to(dev), x=x, X=torch.from_numpy(x).to(dev),
+                  Y=torch.empty(Nh, r1 - r0, device=dev))
 
-        def op_lmhead(r):
-            chk(qmm.qmm_matmul(synth.Q6_K, head_w, Mh, Kh, head_x, Nh, head_y, stream=stream))
+        def op_lmhead(r, hd=hd):   # one copy: 431 MB alone is more than three times L2
+            chk(qmm.qmm_matmul(synth.Q6_K, hd["W"], hd["M"], Kh, hd["X"], Nh, hd["Y"], stream=stream))
         ops["lmhead"], launches_per_pass["lmhead"] = op_lmhead, 1
+        host["lmhead"] = hd
     if "prefill" in only or "prefill_f32" in only:
-        pre_w = [make(synth.Q4_K, M, K, f"bench-prefill-{M}x{K}") for (M, K) in PREFILL_SHAPES]
-        pre_x = [torch.from_numpy(synth.gen_x(PREFILL_N, K, f"bench-prefill-{K}")).to(dev)
-                 for (_, K) in PREFILL_SHAPES]
-        pre_y = [torch.empty(PREFILL_N, M, device=dev) for (M, _) in PREFILL_SHAPES]
-    if "prefill" in only:
-        # bf16 X: the GEMM alone (X in the tensor-core operand type)
-        pre_xb = [torch.from_numpy(synth.f32_to_bf16_bits(x.cpu().numpy())).to(dev).view(torch.bfloat16)
-                  for x in pre_x]
+        pre = []
+        for (M, K) in PREFILL_SHAPES:
+            r0, r1, Mg = local_rows(M, world, rank, args.scaling)
+            w = gen_rows(synth.Q4_K, M, K, f"bench-prefill-{M}x{K}", r0, r1, Mg)
+            x = synth.gen_x(PREFILL_N, K, f"bench-prefill-{K}")
+            xb = synth.f32_to_bf16_bits(x)
+            X = torch.from_numpy(x).to(dev)
+            pre.append(dict(M=r1 - r0, K=K, w=w, W=copies(w), x=x, X=X, xb=xb,
+                            XB=torch.from_numpy(xb).to(dev).view(torch.bfloat16),
+                            ws=qmm.workspace_for(PREFILL_N, K, X),
+                            Y=torch.empty(PREFILL_N, r1 - r0, device=dev),
+                            Y32=torch.empty(PREFILL_N, r1 - r0, device=dev)))
+        host["prefill"] = pre
+        if "prefill" in only:
+            def op_prefill(r):
+                for p in pre:
+                    chk(qmm.qmm_matmul(synth.Q4_K, p["W"][r], p["M"], p["K"], p["XB"], PREFILL_N, p["Y"],
+                                       stream=stream))
+            ops["prefill"], launches_per_pass["prefill"] = op_prefill, len(pre)
+        if "prefill_f32" in only:
+            def op_prefill_f32(r):
+                for p in pre:
+                    chk(qmm.qmm_matmul(synth.Q4_K, p["W"][r], p["M"], p["K"], p["X"], PREFILL_N, p["Y32"], p["ws"],
+                                       stream=stream))
+            ops["prefill_f32"], launches_per_pass["prefill_f32"] = op_prefill_f32, 2 * len(pre)
+    allgather = None
+    if args.allgather and world > 1 and "decode" in only:
+        # the row slices of every decode output, gathered on every rank
+        gat = [torch.empty(world, d["M"], device=dev) for d in host["decode"]]
 
-        def op_prefill(r):
-            for i, (M, K) in enumerate(PREFILL_SHAPES):
-                chk(qmm.qmm_matmul(synth.Q4_K, pre_w[i][r], M, K, pre_xb[i], PREFILL_N, pre_y[i], stream=stream))
-        ops["prefill"], launches_per_pass["prefill"] = op_prefill, len(PREFILL_SHAPES)
-    if "prefill_f32" in only:
-        pre_ws = [qmm.workspace_for(PREFILL_N, K, x) for x, (_, K) in zip(pre_x, PREFILL_SHAPES)]
-
-        def op_prefill_f32(r):
-            for i, (M, K) in enumerate(PREFILL_SHAPES):
-                chk(qmm.qmm_matmul(synth.Q4_K, pre_w[i][r], M, K, pre_x[i], PREFILL_N, pre_y[i], pre_ws[i],
-                                   stream=stream))
-        ops["prefill_f32"], launches_per_pass["prefill_f32"] = op_prefill_f32, 2 * len(PREFILL_SHAPES)
-    rot_bytes = R * sum(wbytes(synth.Q4_0, M, K) for M, K in DECODE_SHAPES)
+        def op_gather(r):
+            for d, g in zip(host["decode"], gat):
+                torch.distributed.all_gather_into_tensor(g, d["Y"].view(-1))
+        allgather = op_gather
     torch.cuda.synchronize()
 
     # warm-up outside capture (also sets kernel attributes): one pass per copy
@@ -258,29 +335,13 @@ def run_gpu(args):
     # one over the first K % R copies, so that exactly K steps are timed.
     K_steps = max(1, args.steps)
     full, rem = divmod(K_steps, R)
-
-    def capture(f, passes):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for r in range(passes):
-                f(r)
-        return g
-
-    graphs = {name: (capture(f, R), capture(f, rem) if rem else None) for name, f in ops.items()}
+    graphs = {name: (Timer(torch, stream, f, R), Timer(torch, stream, f, rem) if rem else None)
+              for name, f in ops.items()}
     torch.cuda.synchronize()
-
-    def replay(g):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            a.record(stream)
-            g.replay()
-            b.record(stream)
-        return a, b
-
     warm_replays = max(1, -(-max(args.warmup, 3) // R))
     for _ in range(warm_replays):
         for name in graphs:
-            replay(graphs[name][0])
+            graphs[name][0].replay()
     torch.cuda.synchronize()
 
     # ---- timed region: exactly K steps; each step = one pass of every op ----
@@ -291,102 +352,136 @@ def run_gpu(args):
     clk.start()
     time.sleep(0.3)
     events = {name: [] for name in graphs}
+    gather_ev = []
     t0 = time.perf_counter()
     for _ in range(full):
         for name in graphs:
-            events[name].append((replay(graphs[name][0]), R))
+            events[name].append(graphs[name][0].replay())
+        if allgather:
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(R):
+                allgather(0)
+            b.record()
+            gather_ev.append((a, b, R))
     if rem:
         for name in graphs:
-            events[name].append((replay(graphs[name][1]), rem))
+            events[name].append(graphs[name][1].replay())
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
     clocks = clk.stop()
     if world > 1:
         torch.distributed.barrier()
 
-    med = {}      # ms per pass (one step of that op), total event time / K
+    med = {}      # ms per step of each op (total event time / K)
     for name, evs in events.items():
-        med[name] = sum(a.elapsed_time(b) for (a, b), _ in evs) / K_steps
-    steps_timed = K_steps
+        med[name] = sum(a.elapsed_time(b) for a, b in evs) / K_steps
+    if gather_ev:
+        med["allgather"] = sum(a.elapsed_time(b) / n for a, b, n in gather_ev) / len(gather_ev)
     med = max_over_ranks(med, world, dev)      # the slowest rank sets the aggregate
     ms_step = sum(med.values())
 
-    dec_bytes = sum(alg_bytes(synth.Q4_0, M, K, 1, 4) for M, K in DECODE_SHAPES)
-    head_bytes = alg_bytes(synth.Q6_K, Mh, Kh, Nh, 4)
-    pre_flops = sum(2.0 * M * K * PREFILL_N for M, K in PREFILL_SHAPES)
-    decode_gbs = dec_bytes / (med["decode"] * 1e-3) / 1e9 * world if "decode" in med else None
-    head_gbs = head_bytes / (med["lmhead"] * 1e-3) / 1e9 * world if "lmhead" in med else None
-    pre_tflops = pre_flops / (med["prefill"] * 1e-3) / 1e12 * world if "prefill" in med else None
-    pre32_tflops = pre_flops / (med["prefill_f32"] * 1e-3) / 1e12 * world if "prefill_f32" in med else None
+    # aggregate algorithmic work over all ranks (global shapes)
+    dec_shape_bytes, dec_t = [], []
+    if "decode" in only:
+        for i, d in enumerate(host["decode"]):
+            Mt = d["M"] * world if args.scaling == "weak" else d["Mg"]
+            dec_shape_bytes.append(alg_bytes(synth.Q4_0, Mt, d["K"], 1, 4))
+            dec_t.append(med[f"decode{i}"])
+        med_decode = sum(dec_t)
+    dec_bytes = sum(dec_shape_bytes)
+    g_lm = Mh * (world if args.scaling == "weak" else 1)
+    head_bytes = alg_bytes(synth.Q6_K, g_lm, Kh, Nh, 4)
+    pre_flops = sum(2.0 * M * K * PREFILL_N for M, K in PREFILL_SHAPES) * (world if args.scaling == "weak" else 1)
+    decode_gbs = dec_bytes / (med_decode * 1e-3) / 1e9 if dec_bytes else None
+    head_gbs = head_bytes / (med["lmhead"] * 1e-3) / 1e9 if "lmhead" in med else None
+    pre_tflops = pre_flops / (med["prefill"] * 1e-3) / 1e12 if "prefill" in med else None
+    pre32_tflops = pre_flops / (med["prefill_f32"] * 1e-3) / 1e12 if "prefill_f32" in med else None
 
-    # dominant kernel of the step -> roofline object
-    shares = {k: v / sum(med.values()) for k, v in med.items()}
+    # ---- other workloads (outside the step time) ----
+    workloads = {} if (args.no_extras or world > 1) else run_workloads(torch, qmm, stream, dev, args, chk)
+
+    # ---- output check on sampled rows against the oracle ----
+    check = None if args.no_check else check_outputs(host, Nh, Kh)
+
+    # per-op rows for the step
+    step_ops = {}
+    if "decode" in only:
+        step_ops["decode"] = med_decode
+    for k in ("lmhead", "prefill", "prefill_f32", "allgather"):
+        if k in med:
+            step_ops[k] = med[k]
+    shares = {k: v / sum(step_ops.values()) for k, v in step_ops.items()}
     dom = max(shares, key=shares.get)
+    gpu_share = {"decode": "gemv_stream_kernel (Q4_0, N=1, 4 shapes)",
+                 "lmhead": "gemv_mma_kernel (Q6_K 128256x4096, N=8)",
+                 "prefill": "gemm_tc_kernel (Q4_K, N=512, bf16 X)",
+                 "prefill_f32": "x_to_bf16_kernel + gemm_tc_kernel (Q4_K, N=512)"}
     if dom in ("prefill", "prefill_f32"):
         tf = pre_tflops if dom == "prefill" else pre32_tflops
         roof = {"bound": "tensor", "achieved": round(tf, 1), "peak": bf16_peak, "unit": "TFLOP/s",
-                "frac": round(tf / bf16_peak, 4), "traffic": traffic_for(dom),
-                "kernel": "gemm_tc (Q4_K, N=512)" + ("" if dom == "prefill" else " + x_to_bf16"),
+                "frac": round(tf / bf16_peak, 4), "traffic": traffic_for(dom), "kernel": gpu_share[dom],
                 "peak_source": f"bf16_tflops ({peak_src})"}
     elif dom == "lmhead":
         roof = {"bound": "hbm", "achieved": round(head_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
                 "frac": round(head_gbs / hbm_peak, 4), "traffic": traffic_for("lmhead"),
-                "kernel": "gemv_mma (Q6_K 128256x4096, N=8)", "peak_source": f"hbm_gbs ({peak_src})"}
+                "kernel": gpu_share["lmhead"], "peak_source": f"hbm_gbs ({peak_src})"}
     else:
         roof = {"bound": "hbm", "achieved": round(decode_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
                 "frac": round(decode_gbs / hbm_peak, 4), "traffic": traffic_for("decode"),
-                "kernel": "gemv_mma (Q4_0, N=1)", "peak_source": f"hbm_gbs ({peak_src})"}
+                "kernel": gpu_share["decode"], "peak_source": f"hbm_gbs ({peak_src})"}
 
     # ---- end to end: host X in, host Y out, through qmm_matmul_host ----
     e2e = None
-    if not args.no_e2e and "decode" in ops:
-        xh = [torch.from_numpy(synth.gen_x(1, K, f"bench-decode-{K}")).pin_memory() for (_, K) in DECODE_SHAPES]
-        yh = [torch.empty(1, M).pin_memory() for (M, _) in DECODE_SHAPES]
-        xd = [torch.empty(1, K, device=dev) for (_, K) in DECODE_SHAPES]
-        yd = [torch.empty(1, M, device=dev) for (M, _) in DECODE_SHAPES]
+    if not args.no_e2e and "decode" in only:
+        dd = host["decode"]
+        xh = [torch.from_numpy(d["x"]).pin_memory() for d in dd]
+        yh = [torch.empty(1, d["M"]).pin_memory() for d in dd]
+        xd = [torch.empty(1, d["K"], device=dev) for d in dd]
+        yd = [torch.empty(1, d["M"], device=dev) for d in dd]
 
         def e2e_pass(r):
-            for i, (M, K) in enumerate(DECODE_SHAPES):
-                chk(qmm.qmm_matmul_host(synth.Q4_0, dec_w[i][r], M, K, xh[i], 1, yh[i], xd[i], yd[i],
+            for i, d in enumerate(dd):
+                chk(qmm.qmm_matmul_host(synth.Q4_0, d["W"][r], d["M"], d["K"], xh[i], 1, yh[i], xd[i], yd[i],
                                         stream=stream))
         with torch.cuda.stream(stream):
             for r in range(R):
                 e2e_pass(r)
         stream.synchronize()
-        g = capture(e2e_pass, R)
-        ts = []
-        for _ in range(max(3, full)):
-            a, b = replay(g)
-            stream.synchronize()
-            ts.append(a.elapsed_time(b) / R)
-        t_e2e = statistics.median(ts)
-        e2e = {"value": round(dec_bytes / (t_e2e * 1e-3) / 1e9 * world, 1), "unit": "GB/s",
-               "h2d_bytes_per_step": sum(K * 4 for _, K in DECODE_SHAPES),
-               "d2h_bytes_per_step": sum(M * 4 for M, _ in DECODE_SHAPES),
+        tm = Timer(torch, stream, e2e_pass, R)
+        t_e2e = tm.median_ms(max(5, full))
+        t_e2e = max_over_ranks({"e2e": t_e2e}, world, dev)["e2e"]
+        e2e = {"value": round(dec_bytes / (t_e2e * 1e-3) / 1e9, 1), "unit": "GB/s",
+               "h2d_bytes_per_step": sum(d["K"] * 4 for d in dd),
+               "d2h_bytes_per_step": sum(d["M"] * 4 for d in dd),
                "ms_per_step": round(t_e2e, 5),
                "path": "qmm_matmul_host (pinned host X -> device, GEMV, device Y -> pinned host)"}
 
-    launches = steps_timed * sum(launches_per_pass.values())
+    launches = K_steps * sum(launches_per_pass.values())
     r1 = lambda v, nd=1: None if v is None else round(v, nd)    # noqa: E731
     value = decode_gbs if decode_gbs is not None else (head_gbs if head_gbs is not None else pre_tflops)
+    full_run = only == set(ALL_OPS)
     line = {
         "metric": METRIC,
         "value": r1(value),
         "unit": "GB/s" if (decode_gbs is not None or head_gbs is not None) else "TFLOP/s",
         "n_gpus": world,
-        "steps": steps_timed,
+        "steps": K_steps,
         "warmup": max(args.warmup, 3),
         "ms_per_step": round(ms_step, 5),
         "higher_is_better": True,
-        "scaling": "weak",
+        "scaling": args.scaling if world > 1 else "weak",
         "vs_baseline": None,
         "dtype": "f32 (GEMV); bf16 x bf16 -> f32 (GEMM)",
         "data": "synthetic (seeded random blocks and N(0,1) activations)",
-        "config": {"workload": WORKLOAD if len(ops) == 3 else f"subset: {sorted(ops)}",
+        "config": {"workload": WORKLOAD if full_run else f"subset: {sorted(only)}",
                    "decode_N": 1, "lmhead_N": Nh, "prefill_N": PREFILL_N,
-                   "weight_copies": R, "static_weights": not args.no_static_weights, "rotating_bytes": rot_bytes, "l2_bytes": l2,
-                   "l2_policy": f"inputs larger than L2: {R} rotating weight copies ({rot_bytes / 2**20:.0f} MiB "
-                                f"for the decode shapes); the 431 MB LM head alone exceeds L2"},
+                   "weight_copies": R, "static_weights": not args.no_static_weights,
+                   "l2_bytes": l2,
+                   "l2_policy": f"inputs larger than L2: {R} rotating device copies of every decode and prefill "
+                                f"weight matrix; the 431 MB LM head alone exceeds L2",
+                   "parallelism": f"row-sharded x{world} ({args.scaling})" if world > 1 else "1 GPU",
+                   "allgather": bool(allgather)},
         "step_share": {k: round(v, 4) for k, v in shares.items()},
         "roofline": roof,
         "cpu_baseline": None,
@@ -398,25 +493,209 @@ def run_gpu(args):
     if decode_gbs is not None:
         line["decode"] = {"GBps": r1(decode_gbs), "frac_of_measured_hbm": round(decode_gbs / hbm_peak, 4),
                           "frac_of_nominal_8TBps": round(decode_gbs / NOMINAL_HBM_GBS, 4),
-                          "us_per_pass": round(med["decode"] * 1e3, 3),
-                          "per_shape_bytes": [alg_bytes(synth.Q4_0, M, K, 1, 4) for M, K in DECODE_SHAPES]}
+                          "us_per_step": round(med_decode * 1e3, 3),
+                          "per_shape": [{"M": M, "K": K, "us": round(t * 1e3, 3), "bytes": b,
+                                         "GBps": round(b / (t * 1e-3) / 1e9, 1),
+                                         "frac_of_measured_hbm": round(b / (t * 1e-3) / 1e9 / hbm_peak, 4)}
+                                        for (M, K), t, b in zip(DECODE_SHAPES, dec_t, dec_shape_bytes)]}
     if head_gbs is not None:
         line["lmhead"] = {"GBps": r1(head_gbs), "frac_of_measured_hbm": round(head_gbs / hbm_peak, 4),
                           "us": round(med["lmhead"] * 1e3, 3), "N": Nh}
     if pre_tflops is not None:
         line["prefill"] = {"TFLOPs": r1(pre_tflops), "frac_of_measured_bf16": round(pre_tflops / bf16_peak, 4),
+                           "frac_of_sustained_bf16": round(pre_tflops / bf16_sus, 4) if bf16_sus else None,
                            "us": round(med["prefill"] * 1e3, 3), "N": PREFILL_N, "x": "bf16",
                            "includes": "tensor-core GEMM"}
     if pre32_tflops is not None:
         line["prefill_f32"] = {"TFLOPs": r1(pre32_tflops), "frac_of_measured_bf16": round(pre32_tflops / bf16_peak, 4),
                                "us": round(med["prefill_f32"] * 1e3, 3), "N": PREFILL_N, "x": "f32",
                                "includes": "f32->bf16 conversion of X + tensor-core GEMM"}
+    if "allgather" in med:
+        line["allgather_us"] = round(med["allgather"] * 1e3, 3)
+    if workloads:
+        line["workloads"] = workloads
+    if check is not None:
+        line["output_check"] = check
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()
+    if check is not None and not check["pass"]:
+        raise SystemExit("output check against the oracle failed")
+
+
+def run_workloads(torch, qmm, stream, dev, args, chk):
+    """The other configurations: timed like the step (graphs over rotating
+    copies), outside the step time."""
+    hbm_peak, bf16_peak, _, _ = peaks()
+    out = {}
+    R = args.copies
+
+    def timed(f, passes, reps=20):
+        with torch.cuda.stream(stream):
+            for r in range(passes):
+                f(r)
+        torch.cuda.synchronize()
+        tm = Timer(torch, stream, f, passes)
+        for _ in range(2):
+            tm.replay()
+        return tm.median_ms(reps)
+
+    # Q8_0 256x512, N=1: 139 KB, latency-bound (L2-resident copies)
+    wt, M, K = synth.Q8_0, 256, 512
+    w = torch.from_numpy(synth.gen_weights(wt, M, K, "bench-q8")).to(dev)
+    Ws = [w] + [w.clone() for _ in range(63)]
+    X = torch.from_numpy(synth.gen_x(1, K, "bench-q8")).to(dev)
+    Y = torch.empty(1, M, device=dev)
+    t = timed(lambda r: chk(qmm.qmm_matmul(wt, Ws[r], M, K, X, 1, Y, stream=stream)), 64)
+    b = alg_bytes(wt, M, K, 1, 4)
+    out["q8_0_256x512_n1"] = {"us": round(t * 1e3, 3), "GBps": round(b / (t * 1e-3) / 1e9, 1),
+                              "note": "latency-bound: 142 KB per call, copies stay in L2"}
+
+    # Q4_K prefill at N = 64 and 256, bf16 X
+    pre = {}
+    for (M, K) in PREFILL_SHAPES:
+        w = torch.from_numpy(synth.gen_weights(synth.Q4_K, M, K, f"bench-prefill-{M}x{K}")).to(dev)
+        pre[(M, K)] = [w] + [w.clone() for _ in range(R - 1)]
+    for N in (64, 256):
+        res = []
+        for (M, K) in PREFILL_SHAPES:
+            x = synth.gen_x(N, K, f"bench-prefill-{K}")
+            XB = torch.from_numpy(synth.f32_to_bf16_bits(x)).to(dev).view(torch.bfloat16)
+            Y = torch.empty(N, M, device=dev)
+            Ws = pre[(M, K)]
+            t = timed(lambda r: chk(qmm.qmm_matmul(synth.Q4_K, Ws[r], M, K, XB, N, Y, stream=stream)), R)
+            fl = 2.0 * M * K * N
+            by = alg_bytes(synth.Q4_K, M, K, N, 2)
+            res.append({"M": M, "K": K, "us": round(t * 1e3, 3), "TFLOPs": round(fl / (t * 1e-3) / 1e12, 1),
+                        "frac_of_measured_bf16": round(fl / (t * 1e-3) / 1e12 / bf16_peak, 4),
+                        "GBps": round(by / (t * 1e-3) / 1e9, 1),
+                        "frac_of_measured_hbm": round(by / (t * 1e-3) / 1e9 / hbm_peak, 4)})
+        out[f"q4_k_prefill_n{N}"] = res
+    del pre
+
+    # LM head at N = 1 and 4
+    Mh, Kh, _ = LMHEAD
+    w = torch.from_numpy(synth.gen_weights(synth.Q6_K, Mh, Kh, "bench-lmhead")).to(dev)
+    for N in (1, 4):
+        X = torch.from_numpy(synth.gen_x(N, Kh, "bench-lmhead")).to(dev)
+        Y = torch.empty(N, Mh, device=dev)
+        t = timed(lambda r: chk(qmm.qmm_matmul(synth.Q6_K, w, Mh, Kh, X, N, Y, stream=stream)), 1, reps=10)
+        b = alg_bytes(synth.Q6_K, Mh, Kh, N, 4)
+        out[f"q6_k_lmhead_n{N}"] = {"us": round(t * 1e3, 3), "GBps": round(b / (t * 1e-3) / 1e9, 1),
+                                    "frac_of_measured_hbm": round(b / (t * 1e-3) / 1e9 / hbm_peak, 4)}
+    del w
+
+    if not args.no_sweep:
+        out["decoder_sweep"] = run_sweep(torch, qmm, stream, dev, args, chk)
+        out["gemv_gemm_crossover"] = run_crossover(torch, qmm, stream, dev, args, chk)
+    return out
+
+
+def run_crossover(torch, qmm, stream, dev, args, chk):
+    """qmm_gemv against qmm_gemm on the seven projections of one decoder layer
+    at the token counts around the dispatcher's threshold (R rotating layer
+    copies): the evidence for QMM_GEMV_MAX_N."""
+    R = max(2, args.copies // 2)
+    Ws = [{name: torch.from_numpy(synth.gen_weights(wt, M, K, f"layer{c}.{name}")).to(dev)
+           for name, wt, M, K in synth.DECODER_LAYER} for c in range(R)]
+    rows = []
+    for N in (2, 4, 8, 12, 16, 24, 32):
+        X = {K: torch.from_numpy(synth.gen_x(N, K, f"xover-{N}-{K}")).to(dev) for K in (4096, 14336)}
+        Ys = {name: torch.empty(N, M, device=dev) for name, _, M, _ in synth.DECODER_LAYER}
+        ws = torch.empty(max(qmm.qmm_gemm_workspace_bytes(N, 14336, qmm.X_F32), 16), dtype=torch.uint8, device=dev)
+        row = {"N": N}
+        for path in ("gemv", "gemm"):
+            if path == "gemv" and N > qmm.GEMV_MAX_N:
+                continue
+
+            def f(r, path=path, N=N, X=X, Ys=Ys, ws=ws):
+                for name, wt, M, K in synth.DECODER_LAYER:
+                    if path == "gemv":
+                        chk(qmm.qmm_gemv(wt, Ws[r][name], M, K, X[K], N, Ys[name], stream=stream))
+                    else:
+                        chk(qmm.qmm_gemm(wt, Ws[r][name], M, K, X[K], N, Ys[name], ws, stream=stream))
+            with torch.cuda.stream(stream):
+                for r in range(R):
+                    f(r)
+            torch.cuda.synchronize()
+            tm = Timer(torch, stream, f, R)
+            tm.replay()
+            row[f"{path}_us"] = round(tm.median_ms(10) * 1e3, 2)
+        rows.append(row)
+    del Ws
+    torch.cuda.empty_cache()
+    return {"layer": "7 projections of one decoder layer", "points": rows}
+
+
+def run_sweep(torch, qmm, stream, dev, args, chk):
+    """32-layer decoder sweep: 224 projections (7 per layer, independently
+    seeded weights per layer) at each N, one CUDA graph per N; tokens/s =
+    N / (time of the 224 matmuls).  X is one N(0,1) draw per (N, K), Y one
+    buffer per projection shape."""
+    hbm_peak, bf16_peak, _, _ = peaks()
+    layers = args.sweep_layers
+    W = {}
+    for layer in range(layers):
+        for name, wt, M, K in synth.DECODER_LAYER:
+            W[(layer, name)] = torch.from_numpy(synth.gen_weights(wt, M, K, f"layer{layer}.{name}")).to(dev)
+    wtot = sum(wbytes(wt, M, K) for _, wt, M, K in synth.DECODER_LAYER) * layers
+    res = []
+    for N in synth.DECODER_NS:
+        X = {K: torch.from_numpy(synth.gen_x(N, K, f"sweep-{N}-{K}")).to(dev) for K in (4096, 14336)}
+        Ys = {name: torch.empty(N, M, device=dev) for name, _, M, _ in synth.DECODER_LAYER}
+        ws = torch.empty(max(qmm.qmm_gemm_workspace_bytes(N, 14336, qmm.X_F32), 16), dtype=torch.uint8, device=dev)
+
+        def f(_r, N=N, X=X, Ys=Ys, ws=ws):
+            for layer in range(layers):
+                for name, wt, M, K in synth.DECODER_LAYER:
+                    chk(qmm.qmm_matmul(wt, W[(layer, name)], M, K, X[K], N, Ys[name], ws, stream=stream))
+        with torch.cuda.stream(stream):
+            f(0)
+        torch.cuda.synchronize()
+        tm = Timer(torch, stream, f, 1)
+        tm.replay()
+        t = tm.median_ms(5)
+        flops = 2.0 * N * sum(M * K for _, _, M, K in synth.DECODER_LAYER) * layers
+        by = wtot + N * 4 * sum(K + M for _, _, M, K in synth.DECODER_LAYER) * layers
+        res.append({"N": N, "ms": round(t, 4), "tokens_per_s": round(N / (t * 1e-3), 1),
+                    "GBps": round(by / (t * 1e-3) / 1e9, 1), "frac_of_measured_hbm": round(by / (t * 1e-3) / 1e9 / hbm_peak, 4),
+                    "TFLOPs": round(flops / (t * 1e-3) / 1e12, 1),
+                    "frac_of_measured_bf16": round(flops / (t * 1e-3) / 1e12 / bf16_peak, 4)})
+        del X, Ys, ws
+    del W
+    torch.cuda.empty_cache()
+    return {"layers": layers, "projections": 7 * layers, "weight_bytes": wtot, "points": res,
+            "aggregate_tokens_per_s": round(sum(p["N"] for p in res) / (sum(p["ms"] for p in res) * 1e-3), 1)}
+
+
+def check_outputs(host, Nh, Kh):
+    """Sampled rows of each op's last output against the oracle's exact sums
+    (GEMV bar 1e-5 S + 1e-6 at N <= 16, GEMM bar 2e-3 S + 1e-5)."""
+    import oracle
+    oracle.build()
+    rng = np.random.default_rng(20261202)
+    res, ok_all = {}, True
+
+    def one(name, wt, w, M, K, x, y, tol):
+        nonlocal ok_all
+        rows = np.sort(rng.choice(M, size=min(48, M), replace=False))
+        Yr, S = oracle.matmul(wt, w, M, K, x, rows=rows)
+        ok, ratio = oracle.within(y[:, rows], Yr, S, *tol)
+        ok_all &= bool(ok)
+        res[name] = {"rows": int(rows.size), "worst_err_over_tol": float(ratio), "pass": bool(ok)}
+
+    for i, d in enumerate(host.get("decode", [])):
+        one(f"decode{i}", synth.Q4_0, d["w"], d["M"], d["K"], d["x"], d["Y"].cpu().numpy(), (1e-5, 1e-6))
+    if "lmhead" in host:
+        hd = host["lmhead"]
+        one("lmhead", synth.Q6_K, hd["w"], hd["M"], Kh, hd["x"], hd["Y"].cpu().numpy(), (1e-5, 1e-6))
+    for i, p in enumerate(host.get("prefill", [])):
+        one(f"prefill{i}", synth.Q4_K, p["w"], p["M"], p["K"], p["xb"], p["Y"].cpu().numpy(), (2e-3, 1e-5))
+        one(f"prefill_f32_{i}", synth.Q4_K, p["w"], p["M"], p["K"], p["x"], p["Y32"].cpu().numpy(), (2e-3, 1e-5))
+    return {"pass": ok_all, "ops": res}
 
 
 # ---------------------------------------------------------------------------
@@ -429,7 +708,8 @@ def cpu_sample_rows(M, frac):
 
 def cpu_baseline(seconds):
     """Time the oracle on the host cores on a bounded sample of the decode
-    workload (a row subset of each shape, N=1), in the same GB/s unit."""
+    workload (a row subset of each shape, N=1), in the same GB/s unit, plus a
+    short timing of each other workload on a row sample."""
     import oracle
     oracle.build()
     cores = os.cpu_count() or 1
@@ -454,9 +734,27 @@ def cpu_baseline(seconds):
             tot_t += time.perf_counter() - t0
             tot_bytes += rows.size * synth.row_bytes(synth.Q4_0, K) + K * 4 + rows.size * 4
         passes += 1
+    other = {}
+    # the other workloads on small row samples (rates per unit of work)
+    for name, wt, M, K, N in (("q8_0_256x512_n1", synth.Q8_0, 256, 512, 1),
+                              ("q4_k_prefill_4096x4096_n64", synth.Q4_K, 4096, 4096, 64),
+                              ("q6_k_lmhead_n8", synth.Q6_K, 128256, 4096, 8)):
+        rows = cpu_sample_rows(M, min(1.0, 128 / M))
+        w = synth.gen_weights(wt, M, K, "cpu-sample") if M * K <= 4096 * 4096 else \
+            synth.gen_weights(wt, 2048, K, "cpu-sample")
+        Mw = M if M * K <= 4096 * 4096 else 2048
+        rows = rows[rows < Mw]
+        x = synth.gen_x(N, K, "cpu-sample")
+        t0 = time.perf_counter()
+        oracle.matmul(wt, w, Mw, K, x, rows=rows)
+        dt = time.perf_counter() - t0
+        other[name] = {"rows": int(rows.size), "s": round(dt, 4),
+                       "GBps": round(rows.size * synth.row_bytes(wt, K) / dt / 1e9, 4),
+                       "GFLOPs": round(2.0 * rows.size * K * N / dt / 1e9, 3)}
     return {"value": round(tot_bytes / tot_t / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": f"{passes} pass(es) over {frac * 100:.2f}% of the rows of each Q4_0 decode shape, N=1; "
-                      f"{tot_t:.1f} s of oracle time (C, f64, {cores} threads)"}
+                      f"{tot_t:.1f} s of oracle time (C, f64, {cores} threads)",
+            "other_workloads_on_row_samples": other}
 
 
 def run_reference(args):
@@ -496,11 +794,27 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip the other workloads")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the 32-layer decoder sweep")
+    ap.add_argument("--sweep-layers", type=int, default=synth.DECODER_LAYERS)
+    ap.add_argument("--no-check", action="store_true", help="skip the output check against the oracle")
     ap.add_argument("--no-static-weights", action="store_true",
                     help="launch every call only after the preceding kernel has finished")
     ap.add_argument("--only", default="",
                     help="comma list of ops to run (decode,lmhead,prefill,prefill_f32); default all")
+    ap.add_argument("--scaling", choices=["weak", "strong"], default="weak",
+                    help="multi-GPU: per-GPU rows fixed (weak) or global rows fixed (strong)")
+    ap.add_argument("--allgather", action="store_true", help="multi-GPU: gather the decode outputs (NCCL)")
     args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.gpus != world:
+        if world == 1 and args.gpus > 1 and "RANK" not in os.environ:
+            # launched without torchrun: start one rank per GPU ourselves
+            cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={args.gpus}",
+                   "--master-addr", "127.0.0.1", "--master-port", os.environ.get("MASTER_PORT", "29517"),
+                   os.path.abspath(__file__)] + sys.argv[1:]
+            raise SystemExit(subprocess.call(cmd))
+        raise SystemExit(f"--gpus {args.gpus} does not match WORLD_SIZE {world}")
     if args.impl == "reference":
         run_reference(args)
     else:

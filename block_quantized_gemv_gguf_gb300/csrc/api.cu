@@ -28,6 +28,9 @@ std::atomic<int> g_static_weights{-1};
 // through the API, take QMM_GEMV_I8 from the environment (default off: on
 // this part it measures no faster than the bf16 kernel).
 std::atomic<int> g_gemv_i8{-1};
+// 16-row-tile tensor-core GEMV for 2 <= N <= QMM_TC_MAX_N: -1 = not set
+// through the API, take QMM_GEMV_TC from the environment (default off).
+std::atomic<int> g_gemv_tc{-1};
 bool gemv_i8_on() {
     const int v = g_gemv_i8.load();
     if (v >= 0) return v != 0;
@@ -126,7 +129,7 @@ struct Settings {
     int gemv_res;     // QMM_GEMV_RESIDENT: 0 disables the resident-X GEMV
     int stream;       // QMM_GEMV_STREAM: 0 disables the streaming N = 1 GEMV
     int stream_warps; // QMM_STREAM_WARPS: warps per CTA of the streaming GEMV (0 = by shared memory)
-    int tc;           // QMM_GEMV_TC: 0 disables the 16-row-tile tensor-core GEMV (N <= 8)
+    int tc;           // QMM_GEMV_TC: 1 enables the 16-row-tile tensor-core GEMV (opt-in, see qmm_set_gemv_tc)
     int tc_warps;     // QMM_TC_WARPS: warps per CTA of that kernel (0 = by shared memory)
     int tc_max_n;     // QMM_TC_MAX_N: largest N it serves (default 4; above, the ring GEMV is faster)
 };
@@ -150,7 +153,7 @@ const Settings &settings() {
         t.stream_warps = env_int("QMM_STREAM_WARPS", 0);
         if (t.stream_warps != 4 && t.stream_warps != 8 && t.stream_warps != 12 && t.stream_warps != 16)
             t.stream_warps = 0;
-        t.tc = env_int("QMM_GEMV_TC", 1) != 0;
+        t.tc = env_int("QMM_GEMV_TC", 0) != 0;
         t.tc_warps = env_int("QMM_TC_WARPS", 0);
         if (t.tc_warps != 4 && t.tc_warps != 8 && t.tc_warps != 16) t.tc_warps = 0;
         t.tc_max_n = env_int("QMM_TC_MAX_N", 4);
@@ -275,15 +278,19 @@ qmm_status gemv_segments(int wt, const SegIn *seg, int nseg, int64_t K, const vo
     bool fast = K % 256 == 0 && row_bytes % 16 == 0 && (uintptr_t)X % 16 == 0 && m_total <= (1ll << 31) - 1;
     for (int i = 0; i < nseg; ++i) fast = fast && (uintptr_t)seg[i].W % 16 == 0;
     if (q8) fast = fast && (uintptr_t)xscales % 16 == 0;
-    if (fast && nseg == 1 && N == 1 && !amax && !q8 && settings().stream) {
+    // an explicit request for the integer kernel (N <= 2) takes precedence
+    const bool want_i8 = !q8 && gemv_i8_on() && N <= 2;
+    if (fast && nseg == 1 && N == 1 && !q8 && !want_i8 && settings().stream) {
         // one token: the streaming kernel, when the shape fits it
         StreamPlan sp{};
         if (plan_gemv_stream(wt, seg[0].M, K, di.num_sms, settings().stream_warps, sp))
             return from_cuda(launch_gemv_stream(wt, sp, static_cast<const uint8_t *>(seg[0].W), seg[0].M, K, X,
-                                                xt == QMM_X_BF16, seg[0].Y, static_weights(), di.status,
-                                                g_wait_limit.load(), st));
+                                                xt == QMM_X_BF16, seg[0].Y, !amax && static_weights(), di.status,
+                                                g_wait_limit.load(), st, amax, idx, val));
     }
-    if (fast && nseg == 1 && N >= 2 && N <= settings().tc_max_n && !amax && !q8 && settings().tc && gemv_tc_unit_bytes(wt)) {
+    const int tc_on = g_gemv_tc.load() >= 0 ? g_gemv_tc.load() : settings().tc;
+    if (fast && nseg == 1 && N >= 2 && N <= settings().tc_max_n && !q8 && !want_i8 && tc_on &&
+        gemv_tc_unit_bytes(wt)) {
         // several tokens: 16-row tiles on the tensor cores, when the shape fits
         TcPlan tp{};
         if (plan_gemv_tc(wt, seg[0].M, K, (int)N, di.num_sms, settings().tc_warps, tp)) {
@@ -299,8 +306,8 @@ qmm_status gemv_segments(int wt, const SegIn *seg, int nseg, int64_t K, const vo
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
                 return QMM_ERR_CUDA;
             return from_cuda(launch_gemv_tc(wt, tp, wmap, static_cast<const uint8_t *>(seg[0].W), seg[0].M, K, X,
-                                            xt == QMM_X_BF16, (int)N, seg[0].Y, static_weights(), di.status,
-                                            g_wait_limit.load(), st));
+                                            xt == QMM_X_BF16, (int)N, seg[0].Y, !amax && static_weights(), di.status,
+                                            g_wait_limit.load(), st, amax, idx, val));
         }
     }
     if (fast) {
@@ -375,9 +382,9 @@ qmm_status gemv_impl(int wt, const void *W, size_t w_bytes, int64_t M, int64_t K
     return gemv_segments(wt, &seg, 1, K, X, xt, N, stream, amax, idx, val);
 }
 
-qmm_status gemm_impl(int wt, const void *W, size_t w_bytes, int64_t M, int64_t K, const void *X, int xt, int64_t N,
-                     float *Y, void *workspace, size_t ws_bytes, void *stream) {
-    int E, B;
+// Every check qmm_gemm makes before it launches anything.
+qmm_status gemm_check(int wt, const void *W, size_t w_bytes, int64_t M, int64_t K, const void *X, int xt, int64_t N,
+                      const float *Y, const void *workspace, size_t ws_bytes, int &E, int &B) {
     qmm_status s = validate(wt, W, w_bytes, M, K, X, xt, N, Y, QMM_GEMM_MAX_N, E, B);
     if (s != QMM_OK) return s;
     const size_t ws_need = qmm_gemm_workspace_bytes(N, K, (qmm_xtype)xt);
@@ -391,6 +398,15 @@ qmm_status gemm_impl(int wt, const void *W, size_t w_bytes, int64_t M, int64_t K
     const int64_t row_bytes = K / E * B;
     if (K % 256 || row_bytes % 16 || (uintptr_t)W % 16 || (uintptr_t)X % 16) return QMM_ERR_UNSUPPORTED;
     if (M > (1ll << 31) - 1 || row_bytes / 2 > (1ll << 31)) return QMM_ERR_UNSUPPORTED;
+    return QMM_OK;
+}
+
+qmm_status gemm_impl(int wt, const void *W, size_t w_bytes, int64_t M, int64_t K, const void *X, int xt, int64_t N,
+                     float *Y, void *workspace, size_t ws_bytes, void *stream) {
+    int E, B;
+    const qmm_status s = gemm_check(wt, W, w_bytes, M, K, X, xt, N, Y, workspace, ws_bytes, E, B);
+    if (s != QMM_OK) return s;
+    const int64_t row_bytes = K / E * B;
     DevInfo di;
     if (!dev_info(di)) return QMM_ERR_CUDA;
     EncodeTiledFn enc = encode_fn();
@@ -511,13 +527,18 @@ qmm_status qmm_gemm(qmm_wtype wt, const void *W, size_t w_bytes, int64_t M, int6
     return gemm_impl(wt, W, w_bytes, M, K, X, xt, N, Y, workspace, ws_bytes, stream);
 }
 
-qmm_status qmm_matmul(qmm_wtype wt, const void *W, size_t w_bytes, int64_t M, int64_t K, const void *X,
-                      qmm_xtype xt, int64_t N, float *Y, void *workspace, size_t ws_bytes, void *stream) {
+// Whether qmm_matmul sends N tokens to the GEMV.
+bool matmul_uses_gemv(int64_t N) {
     const Settings &cfg = settings();
     bool use_gemv = N <= cfg.gemv_max_n;
     if (cfg.force == 1) use_gemv = N <= QMM_GEMV_MAX_N;
     if (cfg.force == 2) use_gemv = false;
-    if (use_gemv) return gemv_impl(wt, W, w_bytes, M, K, X, xt, N, Y, stream);
+    return use_gemv;
+}
+
+qmm_status qmm_matmul(qmm_wtype wt, const void *W, size_t w_bytes, int64_t M, int64_t K, const void *X,
+                      qmm_xtype xt, int64_t N, float *Y, void *workspace, size_t ws_bytes, void *stream) {
+    if (matmul_uses_gemv(N)) return gemv_impl(wt, W, w_bytes, M, K, X, xt, N, Y, stream);
     return gemm_impl(wt, W, w_bytes, M, K, X, xt, N, Y, workspace, ws_bytes, stream);
 }
 
@@ -530,6 +551,17 @@ qmm_status qmm_matmul_host(qmm_wtype wt, const void *W, size_t w_bytes, int64_t 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const size_t xbytes = (size_t)N * (size_t)K * (xt == QMM_X_F32 ? 4 : 2);
     const size_t ybytes = (size_t)N * (size_t)M * 4;
+    // every check the compute call makes, before anything is copied: a bad
+    // argument leaves x_dev, y_dev and Y_host untouched
+    {
+        int E = 0, B = 0;
+        const qmm_status s =
+            matmul_uses_gemv(N)
+                ? validate(wt, W, w_bytes, M, K, x_dev, xt, N, y_dev, QMM_GEMV_MAX_N, E, B)
+                : gemm_check(wt, W, w_bytes, M, K, x_dev, xt, N, y_dev, workspace, ws_bytes, E, B);
+        if (s != QMM_OK) return s;
+        if (overlaps(x_dev, xbytes, W, (size_t)M * (size_t)(K / E) * (size_t)B)) return QMM_ERR_INVALID_ARG;
+    }
     if (cudaMemcpyAsync(x_dev, X_host, xbytes, cudaMemcpyHostToDevice, st) != cudaSuccess) return QMM_ERR_CUDA;
     t_after_copy = true;
     qmm_status s = qmm_matmul(wt, W, w_bytes, M, K, x_dev, xt, N, y_dev, workspace, ws_bytes, stream);
@@ -587,6 +619,8 @@ qmm_status qmm_gemv_swiglu(qmm_wtype wt, const void *Wg, size_t wg_bytes, const 
 }
 
 void qmm_set_gemv_i8(int on) { g_gemv_i8.store(on < 0 ? -1 : (on ? 1 : 0)); }
+
+void qmm_set_gemv_tc(int on) { g_gemv_tc.store(on < 0 ? -1 : (on ? 1 : 0)); }
 
 size_t qmm_q8act_workspace_bytes(int64_t N, int64_t K) {
     if (N < 1 || K < 1) return 0;

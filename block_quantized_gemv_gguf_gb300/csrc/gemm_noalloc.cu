@@ -11,7 +11,9 @@
 // Host code must not use the array's name as a device pointer: in host code
 // it names a host-side stand-in.  Its device address is looked up with
 // cudaGetSymbolAddress, once per device, with that device current, on the
-// first call made on that device, and cached.
+// first call made on that device, and cached.  cudaDeviceReset destroys the
+// array with the context, so the cached address is not valid after it: a
+// process that resets a device must not call this entry point again.
 #include <mutex>
 
 #include "../../include/qmm.h"
@@ -42,7 +44,14 @@ void *scratch_on_current_device() {
 
 extern "C" qmm_status qmm_gemm_noalloc(qmm_wtype wt, const void *W, size_t w_bytes, int64_t M, int64_t K,
                                        const void *X, qmm_xtype xt, int64_t N, float *Y, void *stream) {
-    if (N < 1 || K < 1 || N > QMM_GEMM_MAX_N) return QMM_ERR_INVALID_ARG;
+    // the argument checks of qmm_gemm come first, so that a bad argument is
+    // reported as such whatever the size of X
+    int E = 0, B = 0;
+    if (qmm_block_info(wt, &E, &B) != QMM_OK) return QMM_ERR_INVALID_ARG;
+    if (xt != QMM_X_F32 && xt != QMM_X_BF16) return QMM_ERR_INVALID_ARG;
+    if (!W || !X || !Y) return QMM_ERR_INVALID_ARG;
+    if (N < 1 || K < 1 || M < 1 || N > QMM_GEMM_MAX_N || K % E) return QMM_ERR_INVALID_ARG;
+    if (w_bytes < (size_t)M * (size_t)(K / E) * (size_t)B) return QMM_ERR_INVALID_ARG;
     const size_t need = qmm_gemm_workspace_bytes(N, K, xt);
     if (need > (size_t)QMM_NOALLOC_SCRATCH_BYTES) return QMM_ERR_UNSUPPORTED;   // N*K*2 too large
     if (need == 0) return qmm_gemm(wt, W, w_bytes, M, K, X, xt, N, Y, nullptr, 0, stream);

@@ -33,6 +33,7 @@
 // QMM_ERR_TIMEOUT in the status word.
 #include <atomic>
 
+#include "amax.cuh"
 #include "common.cuh"
 #include "kernels.h"
 
@@ -312,6 +313,7 @@ struct StreamArgs {
     int off_flag;
     unsigned *status;
     uint64_t limit;
+    AmaxOut amax;      // argmax mode when amax.keys is set: no output is stored
 };
 
 __device__ __forceinline__ bool warp_wait(volatile unsigned *abort_flag, uint64_t *bar, uint32_t parity,
@@ -417,6 +419,8 @@ __global__ void __launch_bounds__(512, 1) gemv_stream_kernel(const __grid_consta
 
     const float4 *xs4 = reinterpret_cast<const float4 *>(xs);
     float *__restrict__ Yc = a.Y + r0;
+    const bool amax = a.amax.keys != nullptr;
+    unsigned long long best = 0ull;   // argmax mode: this thread's best (value, row) key
     int done = 0;   // stages of this warp consumed
     for (int j = 0; j < my_nst; ++j) {
         const int slot = warp * S + j % S;
@@ -446,9 +450,12 @@ __global__ void __launch_bounds__(512, 1) gemv_stream_kernel(const __grid_consta
         if (u < nunits && (lane == 0 || kp != key)) {
             const bool starts = key * U >= s * kLanes;
             const bool ends = key * U + U <= (s + 1) * kLanes;
-            if (starts && ends)
-                Yc[key] = v;
-            else
+            if (starts && ends) {
+                if (amax)
+                    amax_fold(best, v, (int)(r0 + key));
+                else
+                    Yc[key] = v;
+            } else
                 part[2 * s + (starts ? 1 : 0)] = v;   // 0: row begun earlier, 1: row continues later
         }
     }
@@ -470,7 +477,22 @@ __global__ void __launch_bounds__(512, 1) gemv_stream_kernel(const __grid_consta
         if (sa == sb) continue;
         float v = part[2 * sa + 1];
         for (int s = sa + 1; s <= sb; ++s) v += part[2 * s];
-        Yc[rl] = v;
+        if (amax)
+            amax_fold(best, v, (int)(r0 + rl));
+        else
+            Yc[rl] = v;
+    }
+    if (amax) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const unsigned long long x = __shfl_xor_sync(0xffffffffu, best, o);
+            best = x > best ? x : best;
+        }
+        if (lane == 0 && best != 0ull) {
+            atomicMax(a.amax.keys, best);
+            __threadfence();
+        }
+        amax_last_cta(a.amax, 1);
     }
 }
 
@@ -485,7 +507,7 @@ int unit_bytes_of(int fmt) {
     }
 }
 
-constexpr int kSmemMax = 232448;
+constexpr int kSmemMax = 232448 - 1024;   // the opt-in maximum, less room for static shared words
 
 // Shared-memory layout for nw warps, S slots, K and up to nst stages.
 struct StreamLayout {
@@ -572,7 +594,8 @@ bool plan_gemv_stream(int fmt, int64_t M, int64_t K, int num_sms, int force_warp
 }
 
 cudaError_t launch_gemv_stream(int fmt, const StreamPlan &p, const uint8_t *W, int64_t M, int64_t K, const void *X,
-                               int xbf16, float *Y, bool pdl, unsigned *status, uint64_t limit, cudaStream_t st) {
+                               int xbf16, float *Y, bool pdl, unsigned *status, uint64_t limit, cudaStream_t st,
+                               unsigned long long *amax_ws, int32_t *idx, float *val) {
     const int64_t rows = (M + p.grid - 1) / p.grid;
     const int64_t nst = (rows * (K / 256) + kLanes - 1) / kLanes;
     const StreamLayout L = stream_layout(fmt, p.warps, p.S, K, nst);
@@ -591,6 +614,7 @@ cudaError_t launch_gemv_stream(int fmt, const StreamPlan &p, const uint8_t *W, i
     a.off_flag = L.off_flag;
     a.status = status;
     a.limit = limit;
+    a.amax = AmaxOut{amax_ws, amax_ws ? reinterpret_cast<unsigned *>(amax_ws + 1) : nullptr, idx, val};
     switch (fmt) {
     case Q8_0: return launch_fmt<Q8_0>(p, a, xbf16, pdl, st);
     case Q4_0: return launch_fmt<Q4_0>(p, a, xbf16, pdl, st);

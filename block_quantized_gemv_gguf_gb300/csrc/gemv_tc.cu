@@ -40,6 +40,7 @@
 // QMM_ERR_TIMEOUT in the status word.
 #include <atomic>
 
+#include "amax.cuh"
 #include "common.cuh"
 #include "kernels.h"
 
@@ -393,6 +394,7 @@ struct TcArgs {
     uint32_t prefetch;     // L2 prefetch budget per CTA (bytes)
     unsigned *status;
     uint64_t limit;
+    AmaxOut amax;          // argmax mode when amax.keys is set: no output is stored
 };
 
 __device__ __forceinline__ bool tc_wait(volatile unsigned *abort_flag, uint64_t *bar, uint32_t parity,
@@ -469,13 +471,18 @@ __global__ void __launch_bounds__(512, 1) gemv_tc_kernel(const __grid_constant__
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + a.off_bar);
     volatile unsigned *abort_flag = reinterpret_cast<volatile unsigned *>(sm + a.off_flag);
     unsigned *smax = reinterpret_cast<unsigned *>(sm + a.off_flag + 16);   // per-token max |x| bits
+    unsigned long long *skey = reinterpret_cast<unsigned long long *>(sm + a.off_flag + 48);   // argmax keys
+    const bool amax = a.amax.keys != nullptr;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < nw * S; ++i) mbar_init(&bars[i], 1);
         *abort_flag = 0u;
         fence_barrier_init();
     }
-    if (threadIdx.x < 8) smax[threadIdx.x] = 0u;
+    if (threadIdx.x < 8) {
+        smax[threadIdx.x] = 0u;
+        skey[threadIdx.x] = 0ull;
+    }
     if (threadIdx.x == 32) {
         prefetch_tensormap(&wmap);
         // the CTA's rows are one contiguous byte range of W: let L2 fetch it now
@@ -593,8 +600,15 @@ __global__ void __launch_bounds__(512, 1) gemv_tc_kernel(const __grid_constant__
                 const int n = 4 * j + t;
                 if (n < N) {
                     const float sc = xscale[2 * n + 1];
-                    if (r < a.M) a.Y[(int64_t)n * a.M + r] = yg[j] * sc;
-                    if (r + 8 < a.M) a.Y[(int64_t)n * a.M + r + 8] = yg8[j] * sc;
+                    if (amax) {
+                        unsigned long long b = 0ull;
+                        if (r < a.M) amax_fold(b, yg[j] * sc, (int)r);
+                        if (r + 8 < a.M) amax_fold(b, yg8[j] * sc, (int)(r + 8));
+                        if (b) atomicMax(&skey[n], b);
+                    } else {
+                        if (r < a.M) a.Y[(int64_t)n * a.M + r] = yg[j] * sc;
+                        if (r + 8 < a.M) a.Y[(int64_t)n * a.M + r + 8] = yg8[j] * sc;
+                    }
                 }
             }
         } else {
@@ -675,8 +689,19 @@ __global__ void __launch_bounds__(512, 1) gemv_tc_kernel(const __grid_constant__
                 if (tau >= (rgl + 1) * U) continue;
                 v += part[(((size_t)rgl * nw + w) * kTR + rr) * 8 + n];
             }
-            a.Y[(int64_t)n * a.M + r] = v * xscale[2 * n + 1];
+            if (amax)
+                atomicMax(&skey[n], amax_key(v * xscale[2 * n + 1], (int)r));
+            else
+                a.Y[(int64_t)n * a.M + r] = v * xscale[2 * n + 1];
         }
+    }
+    if (amax) {
+        __syncthreads();
+        if ((int)threadIdx.x < N && skey[threadIdx.x]) {
+            atomicMax(a.amax.keys + threadIdx.x, skey[threadIdx.x]);
+            __threadfence();
+        }
+        amax_last_cta(a.amax, N);
     }
 }
 
@@ -712,12 +737,12 @@ TcLayout tc_layout(int fmt, int nw, int S, int64_t K, int N, int64_t nrg_min, in
     L.off_bar = (int)o;
     o += (int64_t)nw * S * 8;
     L.off_flag = (int)o;
-    o += 16 + 32;
+    o += 16 + 32 + 64;   // abort flag, per-token max |x|, argmax keys
     L.total = o > (1ll << 30) ? (1 << 30) : (int)o;
     return L;
 }
 
-constexpr int kTcSmemMax = 232448;
+constexpr int kTcSmemMax = 232448 - 1024;   // the opt-in maximum, less room for static shared words
 
 template <int F, int NT, bool XBF16>
 cudaError_t tc_launch_typed(const TcPlan &p, const CUtensorMap &wmap, const TcArgs &a, bool pdl, cudaStream_t st) {
@@ -782,7 +807,7 @@ bool plan_gemv_tc(int fmt, int64_t M, int64_t K, int N, int num_sms, int force_w
 
 cudaError_t launch_gemv_tc(int fmt, const TcPlan &p, const CUtensorMap &wmap, const uint8_t *W, int64_t M, int64_t K,
                            const void *X, int xbf16, int N, float *Y, bool pdl, unsigned *status, uint64_t limit,
-                           cudaStream_t st) {
+                           cudaStream_t st, unsigned long long *amax_ws, int32_t *idx, float *val) {
     const int64_t RG = (M + kTR - 1) / kTR;
     const int64_t nrg_max = (RG + p.grid - 1) / p.grid, nrg_min = RG / p.grid;
     const TcLayout L = tc_layout(fmt, p.warps, p.S, K, N, nrg_min, nrg_max);
@@ -807,6 +832,7 @@ cudaError_t launch_gemv_tc(int fmt, const TcPlan &p, const CUtensorMap &wmap, co
     a.owner = RG / p.grid >= p.warps ? 1 : 0;   // every CTA has at least `warps` groups
     a.status = status;
     a.limit = limit;
+    a.amax = AmaxOut{amax_ws, amax_ws ? reinterpret_cast<unsigned *>(amax_ws + N) : nullptr, idx, val};
     switch (fmt) {
     case Q8_0: return tc_launch_fmt<Q8_0>(p, wmap, a, xbf16, pdl, st);
     case Q4_0: return tc_launch_fmt<Q4_0>(p, wmap, a, xbf16, pdl, st);

@@ -72,8 +72,10 @@ struct StreamPlan {
 bool plan_gemv_stream(int fmt, int64_t M, int64_t K, int num_sms, int force_warps, StreamPlan &p);
 // y[M] = W x.  pdl: programmatic dependent of the preceding kernel (the
 // weight copies start before it ends; X and Y wait for it).
+// amax_ws != nullptr: argmax mode as in launch_gemv_mma (Y is not written).
 cudaError_t launch_gemv_stream(int fmt, const StreamPlan &p, const uint8_t *W, int64_t M, int64_t K, const void *X,
-                               int xbf16, float *Y, bool pdl, unsigned *status, uint64_t limit, cudaStream_t st);
+                               int xbf16, float *Y, bool pdl, unsigned *status, uint64_t limit, cudaStream_t st,
+                               unsigned long long *amax_ws = nullptr, int32_t *idx = nullptr, float *val = nullptr);
 
 // Tensor-core GEMV for 1 <= N <= 8 (mma.sync f16 on the exact codes) of
 // Q8_0 / Q4_0 / Q4_K / Q5_K rows (K % 256 == 0, K <= 32768, 16-byte aligned
@@ -87,9 +89,11 @@ struct TcPlan {
 };
 int gemv_tc_unit_bytes(int fmt);   // 0: format not handled
 bool plan_gemv_tc(int fmt, int64_t M, int64_t K, int N, int num_sms, int force_warps, TcPlan &p);
+// amax_ws != nullptr: argmax mode as in launch_gemv_mma (Y is not written).
 cudaError_t launch_gemv_tc(int fmt, const TcPlan &p, const CUtensorMap &wmap, const uint8_t *W, int64_t M, int64_t K,
                            const void *X, int xbf16, int N, float *Y, bool pdl, unsigned *status, uint64_t limit,
-                           cudaStream_t st);
+                           cudaStream_t st, unsigned long long *amax_ws = nullptr, int32_t *idx = nullptr,
+                           float *val = nullptr);
 
 // Integer tensor-core GEMV (mma.sync m16n8k32 on the weights' integer codes),
 // same weight maps, segments, plans and argmax mode as launch_gemv_mma.

@@ -27,7 +27,7 @@ GEMV_MAX_N, GEMM_MAX_N = 16, 512
 BLOCK = {Q8_0: (32, 34), Q4_0: (32, 18), Q4_K: (256, 144), Q6_K: (256, 210), Q5_K: (256, 176)}
 EXPORTS = ("qmm_gemv", "qmm_gemv_argmax", "qmm_gemv_multi", "qmm_gemm", "qmm_gemm_workspace_bytes", "qmm_matmul", "qmm_matmul_host",
            "qmm_dequant", "qmm_block_info", "qmm_last_device_error", "qmm_status_str",
-           "qmm_set_wait_limit", "qmm_set_static_weights", "qmm_set_gemv_i8", "qmm_quantize_q8_0",
+           "qmm_set_wait_limit", "qmm_set_static_weights", "qmm_set_gemv_i8", "qmm_set_gemv_tc", "qmm_quantize_q8_0",
            "qmm_gemv_preq", "qmm_q8act_workspace_bytes", "qmm_gemv_q8act", "qmm_gemv_swiglu")
 
 _lock = threading.Lock()
@@ -73,6 +73,8 @@ def load() -> ctypes.CDLL:
         lib.qmm_set_static_weights.restype = None
         lib.qmm_set_gemv_i8.argtypes = [ctypes.c_int]
         lib.qmm_set_gemv_i8.restype = None
+        lib.qmm_set_gemv_tc.argtypes = [ctypes.c_int]
+        lib.qmm_set_gemv_tc.restype = None
         lib.qmm_quantize_q8_0.argtypes = [p, ci, i64, i64, p, p, p]
         lib.qmm_gemv_preq.argtypes = [ci, p, sz, i64, i64, p, p, i64, p, p]
         lib.qmm_q8act_workspace_bytes.argtypes = [i64, i64]
@@ -226,6 +228,13 @@ def qmm_set_gemv_i8(on: int) -> None:
     """GEMV kernel for N <= 2 (see include/qmm.h): 1 integer kernel, 0 bf16
     kernel, -1 the environment's choice (QMM_GEMV_I8, default off)."""
     load().qmm_set_gemv_i8(int(on))
+
+
+def qmm_set_gemv_tc(on: int) -> None:
+    """GEMV kernel for 2 <= N <= 4 (see include/qmm.h): 1 the 16-row-tile
+    tensor-core kernel, 0 the ring kernel, -1 the environment's choice
+    (QMM_GEMV_TC, default off)."""
+    load().qmm_set_gemv_tc(int(on))
 
 
 def qmm_quantize_q8_0(X, N, K, scales, quants, stream=None, xt=None) -> int:

@@ -194,7 +194,11 @@ QMM_API qmm_status qmm_gemm(qmm_wtype wt, const void *W, size_t w_bytes, int64_t
  *     and launches nothing; bf16 X needs no scratch and has no extra limit.
  *   - The first call on a device looks up the array's device address for
  *     that device (cudaGetSymbolAddress) and caches it; make that first call
- *     before any stream capture.
+ *     before any stream capture.  cudaDeviceReset invalidates the cached
+ *     address: calling this entry point after a reset of its device is not
+ *     supported.
+ *   - Arguments are checked as qmm_gemm checks them, before the size limit:
+ *     a bad argument returns QMM_ERR_INVALID_ARG whatever N*K.
  *   - All calls share the one array.  Each call rewrites the part it uses
  *     before reading it, so no clearing is needed, but calls whose kernels
  *     overlap on the GPU (different streams, no ordering between them) race
@@ -223,7 +227,11 @@ QMM_API qmm_status qmm_matmul(qmm_wtype wt, const void *W, size_t w_bytes, int64
  * asynchronously on `stream` (pin the host buffers for overlap).  W stays
  * resident in device memory.  x_dev (>= N*K*sizeof(x element) bytes) and
  * y_dev (>= N*M*4 bytes) are caller-provided device staging buffers.  The
- * host output is valid after the stream is synchronized.
+ * host output is valid after the stream is synchronized.  Every argument
+ * check of qmm_matmul (run on x_dev and y_dev), plus x_dev not overlapping
+ * W, is made before the first copy: on an error status nothing has been
+ * copied or launched.  The sizes of x_dev and y_dev cannot be checked
+ * (plain pointers); they are the caller's promise.
  */
 QMM_API qmm_status qmm_matmul_host(qmm_wtype wt, const void *W, size_t w_bytes, int64_t M, int64_t K,
                            const void *X_host, qmm_xtype xt, int64_t N, float *Y_host,
@@ -307,6 +315,22 @@ QMM_API qmm_status qmm_gemv_swiglu(qmm_wtype wt, const void *Wg, size_t wg_bytes
  * outputs.
  */
 QMM_API void qmm_set_gemv_i8(int on);
+
+/*
+ * GEMV kernel choice for 2 <= N <= 4 (QMM_TC_MAX_N, at most 8) on Q8_0,
+ * Q4_0, Q4_K and Q5_K rows: on (1, or QMM_GEMV_TC=1 in the environment)
+ * runs the 16-row-tile tensor-core kernel, which feeds X to mma.sync as two
+ * binary16 pieces of x * 2^-e with one power-of-two scale e per token
+ * (|x - (hi + lo) 2^e| <= 2^-22 |x| + 2^-40 max_k |x|); off (0, the default)
+ * runs the ring kernel, whose bf16 pieces keep the f32 exponent range.
+ * The tensor-core kernel meets the GEMV tolerance unless a token's
+ * activations span more than about 2^39 between entries that meet
+ * non-zero weights (an entry 2^40 below the token's largest is lost); the
+ * default kernels have no such limit.  -1 returns to the environment's
+ * choice.  Process-wide; takes effect at the next call.  The cera pages
+ * have no counterpart: this is a GB300 kernel choice.
+ */
+QMM_API void qmm_set_gemv_tc(int on);
 
 /*
  * Q8_0 activations ("cera 0.5.2 src/backend/cpu.rs",

@@ -1,8 +1,9 @@
 """Multi-rank bench logic on CPU: two gloo ranks (127.0.0.1), no GPU.
 
-Each rank of `bench.py --gpus N` runs the whole step on its own GPU; the
-aggregate time is the slowest rank's, reduced with MAX over all ranks, and
-the reference arm prints from rank 0 only."""
+Each rank of `bench.py --gpus N` runs the step on its own row slices on its
+own GPU; the aggregate time is the slowest rank's, reduced with MAX over all
+ranks, the reference arm prints from rank 0 only, and a --gpus that does not
+match the launch's WORLD_SIZE is an error, not a silent one-GPU run."""
 from __future__ import annotations
 
 import os
@@ -59,7 +60,15 @@ def test_max_over_ranks_single_rank_is_identity():
 
 def test_reference_arm_prints_only_on_rank_zero():
     env = {**os.environ, "RANK": "1", "WORLD_SIZE": "2", "PYTHONPATH": ROOT}
-    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--cpu-seconds", "0.2"],
-                       env=env, capture_output=True, text=True, timeout=300)
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2", "--impl", "reference",
+                        "--cpu-seconds", "0.2"], env=env, capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stderr[-2000:]
     assert r.stdout.strip() == ""
+
+
+def test_gpus_flag_must_match_the_launch():
+    env = {**os.environ, "RANK": "0", "WORLD_SIZE": "2", "PYTHONPATH": ROOT}
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "3", "--impl", "reference",
+                        "--cpu-seconds", "0.2"], env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode != 0
+    assert "does not match WORLD_SIZE" in r.stderr

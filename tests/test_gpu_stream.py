@@ -128,3 +128,38 @@ def test_stream_forced_shapes(env):
                        capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stderr[-3000:]
     assert r.stdout.strip().startswith("OK"), r.stdout[-3000:]
+
+
+def _hard_x(N, K, name):
+    """Blocks with a 1e6 range between their largest and smallest entries,
+    whole blocks 1e-20 or 1e20 times the rest, a zero block, a lone spike."""
+    x = synth.gen_x(N, K, name).astype(np.float64)
+    rng = np.random.default_rng(7)
+    nb = K // 32
+    for n in range(N):
+        for b in rng.choice(nb, size=max(1, nb // 8), replace=False):
+            x[n, 32 * b:32 * b + 32] *= 10.0 ** rng.uniform(-6, 0, 32)
+        x[n, 0:32] = 0.0
+        x[n, 32:64] *= 1e-20
+        x[n, 64:96] *= 1e20
+        x[n, 100] = 3e4
+    return x.astype(np.float32)
+
+
+@pytest.mark.parametrize("wt", [synth.Q8_0, synth.Q4_0, synth.Q4_K, synth.Q6_K, synth.Q5_K],
+                         ids=["Q8_0", "Q4_0", "Q4_K", "Q6_K", "Q5_K"])
+@pytest.mark.parametrize("N", [1, 2, 4])
+def test_hard_values(wt, N):
+    """Hard activations through the default dispatch (this kernel serves
+    N = 1), against the oracle at the GEMV bar."""
+    M, K = 512, 2048
+    w = synth.gen_weights(wt, M, K, "hard")
+    x = _hard_x(N, K, f"hard-{N}")
+    W = torch.from_numpy(w).cuda()
+    X = torch.from_numpy(x).cuda()
+    Y = torch.empty(N, M, device="cuda")
+    assert qmm.qmm_gemv(wt, W, M, K, X, N, Y) == qmm.OK
+    torch.cuda.synchronize()
+    Yr, S = oracle.matmul(wt, w, M, K, x)
+    ok, ratio = oracle.within(Y.cpu().numpy(), Yr, S, *GEMV_TOL)
+    assert ok, f"worst |err|/tol = {ratio:.3g}"
