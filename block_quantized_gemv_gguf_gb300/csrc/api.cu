@@ -401,11 +401,15 @@ qmm_status gemm_check(int wt, const void *W, size_t w_bytes, int64_t M, int64_t 
     return QMM_OK;
 }
 
+// W2 / Y2 (optional): a second matrix of the same shape sharing X, computed
+// in the same launch (checked by the caller).
 qmm_status gemm_impl(int wt, const void *W, size_t w_bytes, int64_t M, int64_t K, const void *X, int xt, int64_t N,
-                     float *Y, void *workspace, size_t ws_bytes, void *stream) {
+                     float *Y, void *workspace, size_t ws_bytes, void *stream, const void *W2 = nullptr,
+                     float *Y2 = nullptr) {
     int E, B;
     const qmm_status s = gemm_check(wt, W, w_bytes, M, K, X, xt, N, Y, workspace, ws_bytes, E, B);
     if (s != QMM_OK) return s;
+    if (W2 && (uintptr_t)W2 % 16) return QMM_ERR_UNSUPPORTED;
     const int64_t row_bytes = K / E * B;
     DevInfo di;
     if (!dev_info(di)) return QMM_ERR_CUDA;
@@ -420,20 +424,21 @@ qmm_status gemm_impl(int wt, const void *W, size_t w_bytes, int64_t M, int64_t K
         if (e != cudaSuccess) return QMM_ERR_CUDA;
         xb = workspace;
     }
-    const int bn = choose_bn(M, N, di.num_sms);
+    const int bn = choose_bn(W2 ? 2 * M : M, N, di.num_sms);
 
-    CUtensorMap wmap, xmap;
-    {
+    CUtensorMap wmap, wmap2, xmap;
+    for (int i = 0; i < (W2 ? 2 : 1); ++i) {
         const int win = gemm_raw_window_bytes(wt);
         cuuint64_t dims[2] = {(cuuint64_t)(row_bytes / 2), (cuuint64_t)M};
         cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
         cuuint32_t box[2] = {(cuuint32_t)(win / 2), 128u};
         cuuint32_t estr[2] = {1u, 1u};
-        if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void *>(W), dims, strides, box, estr,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        if (enc(i ? &wmap2 : &wmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void *>(i ? W2 : W), dims, strides,
+                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return QMM_ERR_CUDA;
     }
+    if (!W2) wmap2 = wmap;
     {
         // {64 k within a block, token, 64-k block}: one copy = XG stages
         cuuint64_t dims[3] = {64u, (cuuint64_t)N, (cuuint64_t)(K / 64)};
@@ -452,10 +457,11 @@ qmm_status gemm_impl(int wt, const void *W, size_t w_bytes, int64_t M, int64_t K
     a.N = (int)N;
     a.bn = bn;
     a.Y = Y;
+    a.Y2 = W2 ? Y2 : nullptr;
     a.status = di.status;
     a.wait_limit = g_wait_limit.load();
     a.pdl = static_weights() ? 1 : 0;
-    return from_cuda(launch_gemm_tc(a, wmap, xmap, st));
+    return from_cuda(launch_gemm_tc(a, wmap, wmap2, xmap, st));
 }
 
 }  // namespace
@@ -665,6 +671,61 @@ qmm_status qmm_gemv_q8act(qmm_wtype wt, const void *W, size_t w_bytes, int64_t M
     s = qmm_quantize_q8_0(X, xt, N, K, sc, q, stream);
     if (s != QMM_OK) return s;
     return qmm_gemv_preq(wt, W, w_bytes, M, K, sc, q, N, Y, stream);
+}
+
+size_t qmm_gemm_q8act_workspace_bytes(int64_t N, int64_t K) {
+    if (N < 1 || K < 1) return 0;
+    return (size_t)N * (size_t)K * 2;
+}
+
+qmm_status qmm_gemm_q8act(qmm_wtype wt, const void *W, size_t w_bytes, int64_t M, int64_t K, const void *X,
+                          qmm_xtype xt, int64_t N, float *Y, void *workspace, size_t ws_bytes, void *stream) {
+    int E, B;
+    // the checks of qmm_gemm on X as given, plus the activation workspace
+    qmm_status s = validate(wt, W, w_bytes, M, K, X, xt, N, Y, QMM_GEMM_MAX_N, E, B);
+    if (s != QMM_OK) return s;
+    const size_t need = qmm_gemm_q8act_workspace_bytes(N, K);
+    const size_t xs = xt == QMM_X_F32 ? 4 : 2;
+    if (!workspace || ws_bytes < need || (uintptr_t)workspace % 16) return QMM_ERR_INVALID_ARG;
+    if (overlaps(workspace, need, Y, (size_t)N * M * 4) || overlaps(workspace, need, X, (size_t)N * K * xs) ||
+        overlaps(workspace, need, W, (size_t)M * (K / E) * B))
+        return QMM_ERR_INVALID_ARG;
+    s = gemm_check(wt, W, w_bytes, M, K, workspace, QMM_X_BF16, N, Y, nullptr, 0, E, B);
+    if (s != QMM_OK) return s;
+    if (launch_quantize_q8_0_bf16(X, xt == QMM_X_BF16, N * K, static_cast<uint16_t *>(workspace), static_weights(),
+                                  static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return QMM_ERR_CUDA;
+    return gemm_impl(wt, W, w_bytes, M, K, workspace, QMM_X_BF16, N, Y, nullptr, 0, stream);
+}
+
+size_t qmm_gemm_swiglu_workspace_bytes(int64_t N, int64_t M, int64_t K, qmm_xtype xt) {
+    if (N < 1 || M < 1 || K < 1) return 0;
+    return (qmm_gemm_workspace_bytes(N, K, xt) + 15) / 16 * 16 + 2 * (size_t)N * (size_t)M * 4;
+}
+
+qmm_status qmm_gemm_swiglu(qmm_wtype wt, const void *Wg, size_t wg_bytes, const void *Wu, size_t wu_bytes, int64_t M,
+                           int64_t K, const void *X, qmm_xtype xt, int64_t N, float *Y, void *workspace,
+                           size_t ws_bytes, void *stream) {
+    int E, B;
+    qmm_status s = validate(wt, Wg, wg_bytes, M, K, X, xt, N, Y, QMM_GEMM_MAX_N, E, B);
+    if (s != QMM_OK) return s;
+    s = validate(wt, Wu, wu_bytes, M, K, X, xt, N, Y, QMM_GEMM_MAX_N, E, B);
+    if (s != QMM_OK) return s;
+    const size_t need = qmm_gemm_swiglu_workspace_bytes(N, M, K, xt);
+    if (!workspace || ws_bytes < need || (uintptr_t)workspace % 16) return QMM_ERR_INVALID_ARG;
+    const size_t wb = (size_t)M * (size_t)(K / E) * (size_t)B, ny = (size_t)N * (size_t)M;
+    const size_t xs = xt == QMM_X_F32 ? 4 : 2;
+    if (overlaps(workspace, need, Wg, wb) || overlaps(workspace, need, Wu, wb) ||
+        overlaps(workspace, need, X, (size_t)N * K * xs) || overlaps(workspace, need, Y, ny * 4))
+        return QMM_ERR_INVALID_ARG;
+    const size_t xws = (qmm_gemm_workspace_bytes(N, K, xt) + 15) / 16 * 16;
+    float *g = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + xws);
+    float *u = g + ny;
+    s = gemm_check(wt, Wg, wg_bytes, M, K, X, xt, N, g, workspace, xws, E, B);
+    if (s != QMM_OK) return s;
+    s = gemm_impl(wt, Wg, wg_bytes, M, K, X, xt, N, g, workspace, xws, stream, Wu, u);
+    if (s != QMM_OK) return s;
+    return from_cuda(launch_swiglu(g, u, (int64_t)ny, Y, static_weights(), static_cast<cudaStream_t>(stream)));
 }
 
 void qmm_set_wait_limit(uint64_t cycles) {

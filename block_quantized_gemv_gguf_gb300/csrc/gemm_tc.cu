@@ -233,8 +233,9 @@ __device__ __forceinline__ void dequant32<Q6_K>(const uint8_t *rb, int sub, int 
 
 template <int F, int BN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap, int M, int K,
-                   int N, float *__restrict__ Y, unsigned *status, uint64_t wait_limit) {
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap wmap2,
+                   const __grid_constant__ CUtensorMap xmap, int M, int K, int N, float *__restrict__ Y1,
+                   float *__restrict__ Y2, unsigned *status, uint64_t wait_limit) {
     using L = Layout<F, BN>;
     constexpr int SA = L::SA, SX = L::SX;
     constexpr int RAWB = Raw<F>::bytes;
@@ -254,13 +255,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     unsigned *abort_flag = reinterpret_cast<unsigned *>(smem + L::OFF_MISC + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.x * BM, n0 = blockIdx.y * BN;
+    // With a second matrix (Y2 set: two projections of the same shape that
+    // share X, e.g. gate and up), the second half of the grid's x range
+    // takes it.
+    const int tiles_m = (M + BM - 1) / BM;
+    const bool second = Y2 != nullptr && (int)blockIdx.x >= tiles_m;
+    const CUtensorMap *wm = second ? &wmap2 : &wmap;
+    float *__restrict__ Y = second ? Y2 : Y1;
+    const int m0 = (second ? (int)blockIdx.x - tiles_m : (int)blockIdx.x) * BM, n0 = blockIdx.y * BN;
     const int nkc = K / KC;
     const int nsteps = nkc * (KC / BK);
     // Each CTA walks K starting at its own chunk (a rotation): CTAs that run
     // in lockstep then read different X tiles at any moment instead of all
     // hitting the same L2 lines at once.  The k-sum is the same set of terms.
-    const int koff = (int)((blockIdx.x * 5u + blockIdx.y * 3u) % (unsigned)nkc);
+    const int koff = (int)(((unsigned)(m0 / BM) * 5u + blockIdx.y * 3u) % (unsigned)nkc);
     auto kchunk = [&](int c) { return c + koff < nkc ? c + koff : c + koff - nkc; };
     const Ctl ctl{abort_flag, wait_limit};
     const uint64_t drain_limit = wait_limit < (1ull << 31) ? (1ull << 31) : wait_limit;
@@ -282,7 +290,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         *abort_flag = 0u;
         fence_barrier_init();
     }
-    if (warp == WARP_WPROD && lane == 0) prefetch_tensormap(&wmap);
+    if (warp == WARP_WPROD && lane == 0) prefetch_tensormap(wm);
     if (warp == WARP_XPROD && lane == 0) prefetch_tensormap(&xmap);
     if (warp == WARP_MMA) {
         tmem_alloc(tmem_slot, L::TMEM_COLS);
@@ -307,7 +315,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 else
                     xb = kchunk(c) * RAWB;
                 mbar_arrive_expect_tx(&raw_full[r], (uint32_t)L::RAW_BYTES);
-                tma_load_2d(sRaw + r * L::RAW_BYTES, &wmap, &raw_full[r], xb >> 1, m0);
+                tma_load_2d(sRaw + r * L::RAW_BYTES, wm, &raw_full[r], xb >> 1, m0);
                 issued = c + 1;
             }
             if (*abort_flag)   // drain: the last load issued into each stage
@@ -447,7 +455,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }
 
 template <int F, int BN>
-cudaError_t launch_one(const GemmArgs &a, const CUtensorMap &wmap, const CUtensorMap &xmap, cudaStream_t st) {
+cudaError_t launch_one(const GemmArgs &a, const CUtensorMap &wmap, const CUtensorMap &wmap2, const CUtensorMap &xmap,
+                       cudaStream_t st) {
     using L = Layout<F, BN>;
     auto kern = gemm_tc_kernel<F, BN>;
     static std::atomic<uint64_t> configured{0};   // one bit per device ordinal
@@ -462,7 +471,7 @@ cudaError_t launch_one(const GemmArgs &a, const CUtensorMap &wmap, const CUtenso
     }
     cudaLaunchConfig_t cfg = {};
     const int64_t tiles_m = (a.M + BM - 1) / BM;
-    cfg.gridDim = dim3((unsigned)tiles_m, (unsigned)((a.N + BN - 1) / BN), 1);
+    cfg.gridDim = dim3((unsigned)(tiles_m * (a.Y2 ? 2 : 1)), (unsigned)((a.N + BN - 1) / BN), 1);
     cfg.blockDim = dim3(NUM_THREADS, 1, 1);
     cfg.dynamicSmemBytes = L::SMEM;
     cfg.stream = st;
@@ -475,17 +484,19 @@ cudaError_t launch_one(const GemmArgs &a, const CUtensorMap &wmap, const CUtenso
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    e = cudaLaunchKernelEx(&cfg, kern, wmap, xmap, (int)a.M, (int)a.K, a.N, a.Y, a.status, a.wait_limit);
+    e = cudaLaunchKernelEx(&cfg, kern, wmap, wmap2, xmap, (int)a.M, (int)a.K, a.N, a.Y, a.Y2, a.status,
+                           a.wait_limit);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
 template <int F>
-cudaError_t launch_fmt(const GemmArgs &a, const CUtensorMap &wmap, const CUtensorMap &xmap, cudaStream_t st) {
+cudaError_t launch_fmt(const GemmArgs &a, const CUtensorMap &wmap, const CUtensorMap &wmap2, const CUtensorMap &xmap,
+                       cudaStream_t st) {
     switch (a.bn) {
-    case 64: return launch_one<F, 64>(a, wmap, xmap, st);
-    case 128: return launch_one<F, 128>(a, wmap, xmap, st);
-    case 256: return launch_one<F, 256>(a, wmap, xmap, st);
+    case 64: return launch_one<F, 64>(a, wmap, wmap2, xmap, st);
+    case 128: return launch_one<F, 128>(a, wmap, wmap2, xmap, st);
+    case 256: return launch_one<F, 256>(a, wmap, wmap2, xmap, st);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -505,13 +516,14 @@ int gemm_raw_window_bytes(int fmt) {
     }
 }
 
-cudaError_t launch_gemm_tc(const GemmArgs &a, const CUtensorMap &wmap, const CUtensorMap &xmap, cudaStream_t st) {
+cudaError_t launch_gemm_tc(const GemmArgs &a, const CUtensorMap &wmap, const CUtensorMap &wmap2, const CUtensorMap &xmap,
+                           cudaStream_t st) {
     switch (a.fmt) {
-    case Q8_0: return launch_fmt<Q8_0>(a, wmap, xmap, st);
-    case Q4_0: return launch_fmt<Q4_0>(a, wmap, xmap, st);
-    case Q4_K: return launch_fmt<Q4_K>(a, wmap, xmap, st);
-    case Q6_K: return launch_fmt<Q6_K>(a, wmap, xmap, st);
-    case Q5_K: return launch_fmt<Q5_K>(a, wmap, xmap, st);
+    case Q8_0: return launch_fmt<Q8_0>(a, wmap, wmap2, xmap, st);
+    case Q4_0: return launch_fmt<Q4_0>(a, wmap, wmap2, xmap, st);
+    case Q4_K: return launch_fmt<Q4_K>(a, wmap, wmap2, xmap, st);
+    case Q6_K: return launch_fmt<Q6_K>(a, wmap, wmap2, xmap, st);
+    case Q5_K: return launch_fmt<Q5_K>(a, wmap, wmap2, xmap, st);
     default: return cudaErrorInvalidValue;
     }
 }

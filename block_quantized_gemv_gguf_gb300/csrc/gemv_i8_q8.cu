@@ -12,9 +12,13 @@ namespace {
 // rint(x * id) clamped to [-128, 127] with NaN -> 0, scale = d through
 // binary16.  Division, reciprocal and product are correctly rounded, so the
 // codes and scales are those of any IEEE float implementation.
-template <bool XBF16>
+// BF16OUT: instead of codes and scales, write the dequantized activation
+// bf16(scale * code) (scale * code is exact in f32: 11 x 8 bits), the X
+// operand of the tensor-core GEMM on Q8_0 activations.
+template <bool XBF16, bool BF16OUT>
 __global__ void __launch_bounds__(256) quantize_q8_0_kernel(const void *__restrict__ Xv, int64_t nblocks,
-                                                             float *__restrict__ scales, int8_t *__restrict__ quants) {
+                                                             float *__restrict__ scales, int8_t *__restrict__ quants,
+                                                             __nv_bfloat16 *__restrict__ xq) {
     const int lane = threadIdx.x & 31;
     pdl_launch_dependents();
     pdl_wait();   // X may come from the preceding kernel
@@ -33,8 +37,13 @@ __global__ void __launch_bounds__(256) quantize_q8_0_kernel(const void *__restri
         const float id = (d != 0.0f && isfinite(r)) ? r : 0.0f;
         float q = rintf(__fmul_rn(v, id));
         q = isnan(q) ? 0.0f : fminf(fmaxf(q, -128.0f), 127.0f);
-        quants[b * 32 + lane] = (int8_t)(int)q;
-        if (lane == 0) scales[b] = __half2float(__float2half_rn(d));
+        const float dh = __half2float(__float2half_rn(d));
+        if constexpr (BF16OUT) {
+            xq[b * 32 + lane] = __float2bfloat16_rn(dh * q);
+        } else {
+            quants[b * 32 + lane] = (int8_t)(int)q;
+            if (lane == 0) scales[b] = dh;
+        }
     }
 }
 
@@ -68,8 +77,9 @@ int maxc_f(int N, int rows) {
 
 }  // namespace
 
-cudaError_t launch_quantize_q8_0(const void *X, int xbf16, int64_t count, float *scales, int8_t *quants, bool pdl,
-                                 cudaStream_t st) {
+namespace {
+cudaError_t launch_quant(const void *X, int xbf16, int64_t count, float *scales, int8_t *quants, uint16_t *xq,
+                         bool pdl, cudaStream_t st) {
     const int64_t nblocks = count / 32;
     if (nblocks <= 0) return cudaSuccess;
     int64_t grid = (nblocks + 7) / 8;
@@ -83,10 +93,27 @@ cudaError_t launch_quantize_q8_0(const void *X, int xbf16, int64_t count, float 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    const cudaError_t e = xbf16 ? cudaLaunchKernelEx(&cfg, quantize_q8_0_kernel<true>, X, nblocks, scales, quants)
-                                : cudaLaunchKernelEx(&cfg, quantize_q8_0_kernel<false>, X, nblocks, scales, quants);
+    __nv_bfloat16 *o = reinterpret_cast<__nv_bfloat16 *>(xq);
+    cudaError_t e;
+    if (xq)
+        e = xbf16 ? cudaLaunchKernelEx(&cfg, quantize_q8_0_kernel<true, true>, X, nblocks, scales, quants, o)
+                  : cudaLaunchKernelEx(&cfg, quantize_q8_0_kernel<false, true>, X, nblocks, scales, quants, o);
+    else
+        e = xbf16 ? cudaLaunchKernelEx(&cfg, quantize_q8_0_kernel<true, false>, X, nblocks, scales, quants, o)
+                  : cudaLaunchKernelEx(&cfg, quantize_q8_0_kernel<false, false>, X, nblocks, scales, quants, o);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_quantize_q8_0(const void *X, int xbf16, int64_t count, float *scales, int8_t *quants, bool pdl,
+                                 cudaStream_t st) {
+    return launch_quant(X, xbf16, count, scales, quants, nullptr, pdl, st);
+}
+
+cudaError_t launch_quantize_q8_0_bf16(const void *X, int xbf16, int64_t count, uint16_t *out, bool pdl,
+                                      cudaStream_t st) {
+    return launch_quant(X, xbf16, count, nullptr, nullptr, out, pdl, st);
 }
 
 int gemv_i8_q8_maxc(int fmt, int N, int rows) {

@@ -114,8 +114,12 @@ cudaError_t launch_gemv_i8_q8(int fmt, const GemvPlan &plan, const GemvSegs &seg
 
 // Q8_0 activations of X (f32 or bf16, count % 32 == 0): scales[count/32],
 // quants[count].  pdl: programmatic dependent of the preceding kernel.
+// launch_quantize_q8_0_bf16: the same quantizer, writing instead
+// out[i] = bf16(scale * code) (the dequantized activation, rounded to bf16).
 cudaError_t launch_quantize_q8_0(const void *X, int xbf16, int64_t count, float *scales, int8_t *quants, bool pdl,
                                  cudaStream_t st);
+cudaError_t launch_quantize_q8_0_bf16(const void *X, int xbf16, int64_t count, uint16_t *out, bool pdl,
+                                      cudaStream_t st);
 
 // K split of a GEMV over `tiles` row tiles: the smallest power of two (<= 8)
 // giving at least 1.5 CTAs per SM, and (max_cps > 0) slices of at most
@@ -146,11 +150,15 @@ struct GemmArgs {
     int N;
     int bn;          // token tile (64, 128 or 256)
     float *Y;
+    float *Y2;       // second matrix's output (wmap2; same M and K), or null
     unsigned *status;
     uint64_t wait_limit;
     int pdl;         // programmatic dependent launch (weights read before the preceding kernel ends)
 };
-cudaError_t launch_gemm_tc(const GemmArgs &a, const CUtensorMap &wmap, const CUtensorMap &xmap, cudaStream_t st);
+// With a.Y2 set, one launch computes two matrices of the same shape that
+// share X (wmap -> Y, wmap2 -> Y2); otherwise wmap2 is not read.
+cudaError_t launch_gemm_tc(const GemmArgs &a, const CUtensorMap &wmap, const CUtensorMap &wmap2,
+                           const CUtensorMap &xmap, cudaStream_t st);
 
 int gemm_x_stages_per_copy(int bn);
 

@@ -28,7 +28,8 @@ BLOCK = {Q8_0: (32, 34), Q4_0: (32, 18), Q4_K: (256, 144), Q6_K: (256, 210), Q5_
 EXPORTS = ("qmm_gemv", "qmm_gemv_argmax", "qmm_gemv_multi", "qmm_gemm", "qmm_gemm_workspace_bytes", "qmm_matmul", "qmm_matmul_host",
            "qmm_dequant", "qmm_block_info", "qmm_last_device_error", "qmm_status_str",
            "qmm_set_wait_limit", "qmm_set_static_weights", "qmm_set_gemv_i8", "qmm_set_gemv_tc", "qmm_quantize_q8_0",
-           "qmm_gemv_preq", "qmm_q8act_workspace_bytes", "qmm_gemv_q8act", "qmm_gemv_swiglu")
+           "qmm_gemv_preq", "qmm_q8act_workspace_bytes", "qmm_gemv_q8act", "qmm_gemv_swiglu",
+           "qmm_gemm_q8act_workspace_bytes", "qmm_gemm_q8act", "qmm_gemm_swiglu_workspace_bytes", "qmm_gemm_swiglu")
 
 _lock = threading.Lock()
 _lib = None
@@ -81,8 +82,15 @@ def load() -> ctypes.CDLL:
         lib.qmm_q8act_workspace_bytes.restype = sz
         lib.qmm_gemv_q8act.argtypes = [ci, p, sz, i64, i64, p, ci, i64, p, p, sz, p]
         lib.qmm_gemv_swiglu.argtypes = [ci, p, sz, p, sz, i64, i64, p, ci, i64, p, p, sz, p]
+        lib.qmm_gemm_q8act_workspace_bytes.argtypes = [i64, i64]
+        lib.qmm_gemm_q8act_workspace_bytes.restype = sz
+        lib.qmm_gemm_q8act.argtypes = [ci, p, sz, i64, i64, p, ci, i64, p, p, sz, p]
+        lib.qmm_gemm_swiglu_workspace_bytes.argtypes = [i64, i64, i64, ci]
+        lib.qmm_gemm_swiglu_workspace_bytes.restype = sz
+        lib.qmm_gemm_swiglu.argtypes = [ci, p, sz, p, sz, i64, i64, p, ci, i64, p, p, sz, p]
         for f in ("qmm_gemv", "qmm_gemv_argmax", "qmm_gemv_multi", "qmm_gemm", "qmm_matmul", "qmm_matmul_host", "qmm_dequant", "qmm_block_info",
-                  "qmm_last_device_error", "qmm_quantize_q8_0", "qmm_gemv_preq", "qmm_gemv_q8act", "qmm_gemv_swiglu"):
+                  "qmm_last_device_error", "qmm_quantize_q8_0", "qmm_gemv_preq", "qmm_gemv_q8act", "qmm_gemv_swiglu",
+                  "qmm_gemm_q8act", "qmm_gemm_swiglu"):
             getattr(lib, f).restype = ci
         _lib = lib
         return lib
@@ -270,6 +278,40 @@ def gemv_swiglu(wt, Wg, Wu, M, K, X, Y=None, workspace=None, stream=None):
     if workspace is None:
         workspace = torch.empty(2 * N * M, dtype=torch.float32, device=X.device)
     _check(qmm_gemv_swiglu(wt, Wg, Wu, M, K, X, N, Y, workspace, stream), "qmm_gemv_swiglu")
+    return Y
+
+
+def qmm_gemm_q8act(wt, W, M, K, X, N, Y, workspace, stream=None, w_bytes=None, xt=None) -> int:
+    return load().qmm_gemm_q8act(wt, _ptr(W), _nbytes(W) if w_bytes is None else w_bytes, M, K, _ptr(X),
+                                 _xtype(X) if xt is None else xt, N, _ptr(Y), _ptr(workspace), _nbytes(workspace),
+                                 _stream(stream))
+
+
+def gemm_q8act(wt, W, M, K, X, Y=None, workspace=None, stream=None):
+    """Y [N, M]: the tensor-core GEMM on the Q8_0-quantized activations of X."""
+    N = _shape(X, K)
+    Y = torch.empty((N, M), dtype=torch.float32, device=X.device) if Y is None else Y
+    if workspace is None:
+        workspace = torch.empty(load().qmm_gemm_q8act_workspace_bytes(N, K), dtype=torch.uint8, device=X.device)
+    _check(qmm_gemm_q8act(wt, W, M, K, X, N, Y, workspace, stream=stream), "qmm_gemm_q8act")
+    return Y
+
+
+def qmm_gemm_swiglu(wt, Wg, Wu, M, K, X, N, Y, workspace, stream=None, xt=None) -> int:
+    return load().qmm_gemm_swiglu(wt, _ptr(Wg), _nbytes(Wg), _ptr(Wu), _nbytes(Wu), M, K, _ptr(X),
+                                  _xtype(X) if xt is None else xt, N, _ptr(Y), _ptr(workspace), _nbytes(workspace),
+                                  _stream(stream))
+
+
+def gemm_swiglu(wt, Wg, Wu, M, K, X, Y=None, workspace=None, stream=None):
+    """silu(X Wg^T) * (X Wu^T), [N, M], on the tensor-core GEMM (one launch
+    for both projections)."""
+    N = _shape(X, K)
+    Y = torch.empty((N, M), dtype=torch.float32, device=X.device) if Y is None else Y
+    if workspace is None:
+        n = load().qmm_gemm_swiglu_workspace_bytes(N, M, K, _xtype(X))
+        workspace = torch.empty(n, dtype=torch.uint8, device=X.device)
+    _check(qmm_gemm_swiglu(wt, Wg, Wu, M, K, X, N, Y, workspace, stream), "qmm_gemm_swiglu")
     return Y
 
 

@@ -377,6 +377,46 @@ QMM_API qmm_status qmm_gemv_q8act(qmm_wtype wt, const void *W, size_t w_bytes, i
                                   const void *X, qmm_xtype xt, int64_t N, float *Y, void *workspace,
                                   size_t ws_bytes, void *stream);
 
+/*
+ * Prefill on Q8_0 activations, 1 <= N <= QMM_GEMM_MAX_N: the arithmetic of
+ * the pages' batched path ("cera 0.5.2 src/backend/cpu.rs",
+ * gemm_preq_dispatch after quantize_f32_to_q8_0_into: every 32-element block
+ * of each token quantized to Q8_0, then the weights against the quantized
+ * activations).  X[N][K] (f32 or bf16) is quantized exactly as
+ * qmm_quantize_q8_0 does, each activation is replaced by bf16(scale * code)
+ * (scale * code is exact in f32, then rounded once to bf16) in `workspace`
+ * (>= qmm_gemm_q8act_workspace_bytes(N, K) = N*K*2 bytes, 16-byte aligned,
+ * not overlapping W, X or Y), and the tensor-core GEMM of qmm_gemm runs on
+ * it.  Y[N][M] f32, overwritten.  Reference: the exact projection of
+ * dequant(W) on the dequantized activations; tolerance that of qmm_gemm
+ * (2e-3 * sum|w x_q| + 1e-5).  Needs qmm_gemm's geometry (K % 256 == 0,
+ * 16-byte aligned rows and W), else QMM_ERR_UNSUPPORTED.  Two kernels,
+ * asynchronous on `stream`; nothing is written on an error status.
+ */
+QMM_API size_t qmm_gemm_q8act_workspace_bytes(int64_t N, int64_t K);
+QMM_API qmm_status qmm_gemm_q8act(qmm_wtype wt, const void *W, size_t w_bytes, int64_t M, int64_t K,
+                                  const void *X, qmm_xtype xt, int64_t N, float *Y, void *workspace,
+                                  size_t ws_bytes, void *stream);
+
+/*
+ * Gate/up projections with the SwiGLU product on the tensor-core GEMM,
+ * 1 <= N <= QMM_GEMM_MAX_N ("cera 0.5.2 src/backend/cpu.rs",
+ * gemv_q4_0_gate_up_swiglu_with_q8 and silu_mul_inplace, for prefill):
+ * Y[n, m] = silu(g) * u with g = X Wg^T, u = X Wu^T, two M x K matrices of
+ * format wt sharing X.  One GEMM launch computes both projections (its grid
+ * covers the row tiles of Wg and then those of Wu; X is converted to bf16
+ * once when it is f32), then a programmatically dependent kernel writes Y.
+ * workspace (device, 16-byte aligned, >= qmm_gemm_swiglu_workspace_bytes):
+ * the bf16 X (f32 X only, padded to 16 bytes), then g [N][M] and u [N][M]
+ * (left there).  g and u meet the qmm_gemm tolerance; Y carries it through
+ * the activation.  Same geometry requirements as qmm_gemm; no buffer may
+ * overlap another.
+ */
+QMM_API size_t qmm_gemm_swiglu_workspace_bytes(int64_t N, int64_t M, int64_t K, qmm_xtype xt);
+QMM_API qmm_status qmm_gemm_swiglu(qmm_wtype wt, const void *Wg, size_t wg_bytes, const void *Wu,
+                                   size_t wu_bytes, int64_t M, int64_t K, const void *X, qmm_xtype xt,
+                                   int64_t N, float *Y, void *workspace, size_t ws_bytes, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
