@@ -608,7 +608,7 @@ def run_crossover(torch, qmm, stream, dev, args, chk):
         ws = torch.empty(max(qmm.qmm_gemm_workspace_bytes(N, 14336, qmm.X_F32), 16), dtype=torch.uint8, device=dev)
         row = {"N": N}
         for path in ("gemv", "gemm"):
-            if path == "gemv" and N > qmm.GEMV_MAX_N:
+            if path == "gemv" and N > qmm.GEMV_MAX_N:   # the GEMV's own limit
                 continue
 
             def f(r, path=path, N=N, X=X, Ys=Ys, ws=ws):
@@ -790,7 +790,7 @@ def main():
     ap.add_argument("--steps", type=int, default=64)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--copies", type=int, default=8, help="rotating weight copies (inputs > L2)")
+    ap.add_argument("--copies", type=int, default=32, help="rotating weight copies (inputs > L2)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")

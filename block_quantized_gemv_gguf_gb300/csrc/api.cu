@@ -136,7 +136,7 @@ struct Settings {
 const Settings &settings() {
     static Settings s = [] {
         Settings t;
-        t.gemv_max_n = env_int("QMM_GEMV_MAX_N", QMM_GEMV_MAX_N);
+        t.gemv_max_n = env_int("QMM_GEMV_MAX_N", QMM_MATMUL_GEMV_MAX_N);
         if (t.gemv_max_n < 0) t.gemv_max_n = 0;
         if (t.gemv_max_n > QMM_GEMV_MAX_N) t.gemv_max_n = QMM_GEMV_MAX_N;
         const char *f = std::getenv("QMM_FORCE_PATH");

@@ -94,6 +94,11 @@ typedef enum {
  * ("cera 0.3.1 src/model/gpu_lfm2.rs", MAX_PREFILL_TOKENS). */
 #define QMM_GEMV_MAX_N 16
 #define QMM_GEMM_MAX_N 512
+/* Largest N qmm_matmul sends to the GEMV by default (the environment
+ * variable QMM_GEMV_MAX_N can lower it): measured on GB300 over the seven
+ * projections of one decoder layer, the GEMV is faster up to N = 12 and the
+ * GEMM is as fast from N = 16. */
+#define QMM_MATMUL_GEMV_MAX_N 15
 
 /*
  * Multi-token GEMV, 1 <= N <= QMM_GEMV_MAX_N: decode (N = 1) and small-N
@@ -213,8 +218,8 @@ QMM_API qmm_status qmm_gemm_noalloc(qmm_wtype wt, const void *W, size_t w_bytes,
 QMM_API size_t qmm_gemm_workspace_bytes(int64_t N, int64_t K, qmm_xtype xt);
 
 /*
- * N-based dispatcher, 1 <= N <= QMM_GEMM_MAX_N: N <= QMM_GEMV_MAX_N runs
- * qmm_gemv, larger N runs qmm_gemm.  Same arguments as qmm_gemm (the
+ * N-based dispatcher, 1 <= N <= QMM_GEMM_MAX_N: N <= QMM_MATMUL_GEMV_MAX_N
+ * runs qmm_gemv (its tolerance), larger N runs qmm_gemm (its tolerance).  Same arguments as qmm_gemm (the
  * workspace is only touched on the GEMM path).
  */
 QMM_API qmm_status qmm_matmul(qmm_wtype wt, const void *W, size_t w_bytes, int64_t M, int64_t K,

@@ -1,6 +1,6 @@
 """qmm_matmul_host: X from pinned host memory, Y back to it, through the C ABI.
 
-Checks the result against the oracle (GEMV bar at N <= 16, GEMM bar above)
+Checks the result against the oracle (GEMV bar where qmm_matmul takes the GEMV, GEMM bar above)
 and that an invalid argument returns before anything is copied: the device
 staging buffers and the host output keep their poison.
 """
@@ -37,7 +37,7 @@ def test_host_buffers_match_oracle(N):
     assert s == qmm.OK, qmm.status_name(s)
     torch.cuda.synchronize()
     Yr, S = oracle.matmul(wt, w, M, K, x)
-    tol = (1e-5, 1e-6) if N <= qmm.GEMV_MAX_N else (2e-3, 1e-5)
+    tol = (1e-5, 1e-6) if N <= qmm.MATMUL_GEMV_MAX_N else (2e-3, 1e-5)
     ok, ratio = oracle.within(Yh.numpy(), Yr, S, *tol)
     assert ok, f"worst |err|/tol = {ratio:.3g}"
 

@@ -253,8 +253,8 @@ def test_dispatcher(N):
     w = synth.gen_weights(wt, M, K, "disp")
     x = synth.gen_x(N, K, "disp")
     y = run("matmul", wt, w, M, K, x)
-    # N <= 16 takes the f32 GEMV and must meet the tighter bar
-    check(y, w, wt, M, K, x, GEMV_TOL if N <= 16 else GEMM_TOL)
+    # N <= QMM_MATMUL_GEMV_MAX_N takes the f32 GEMV and must meet the tighter bar
+    check(y, w, wt, M, K, x, GEMV_TOL if N <= qmm.MATMUL_GEMV_MAX_N else GEMM_TOL)
 
 
 # --------------------------------------------------------------------------
