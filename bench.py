@@ -191,12 +191,15 @@ class Timer:
     """CUDA graph of `passes` passes of f over rotating inputs; replays timed
     with CUDA events on the launching stream."""
 
-    def __init__(self, torch, stream, f, passes):
+    def __init__(self, torch, stream, f, passes, counter=None):
         self.torch, self.stream, self.passes = torch, stream, passes
         self.g = torch.cuda.CUDAGraph()
+        n0 = counter() if counter else 0
         with torch.cuda.graph(self.g, stream=stream):
             for r in range(passes):
                 f(r)
+        # library kernels recorded into the graph, per pass
+        self.launches = (counter() - n0) / passes if counter else None
 
     def replay(self):
         t = self.torch
@@ -274,7 +277,7 @@ def run_gpu(args):
         for i, d in enumerate(dec):
             def op(r, d=d):
                 chk(qmm.qmm_matmul(synth.Q4_0, d["W"][r], d["M"], d["K"], d["X"], 1, d["Y"], stream=stream))
-            ops[f"decode{i}"], launches_per_pass[f"decode{i}"] = op, 1
+            ops[f"decode{i}"] = op
         host["decode"] = dec
     if "lmhead" in only:
         r0, r1, Mg = local_rows(Mh, world, rank, args.scaling)
@@ -285,7 +288,7 @@ def run_gpu(args):
 
         def op_lmhead(r, hd=hd):   # one copy: 431 MB alone is more than three times L2
             chk(qmm.qmm_matmul(synth.Q6_K, hd["W"], hd["M"], Kh, hd["X"], Nh, hd["Y"], stream=stream))
-        ops["lmhead"], launches_per_pass["lmhead"] = op_lmhead, 1
+        ops["lmhead"] = op_lmhead
         host["lmhead"] = hd
     if "prefill" in only or "prefill_f32" in only:
         pre = []
@@ -306,13 +309,13 @@ def run_gpu(args):
                 for p in pre:
                     chk(qmm.qmm_matmul(synth.Q4_K, p["W"][r], p["M"], p["K"], p["XB"], PREFILL_N, p["Y"],
                                        stream=stream))
-            ops["prefill"], launches_per_pass["prefill"] = op_prefill, len(pre)
+            ops["prefill"] = op_prefill
         if "prefill_f32" in only:
             def op_prefill_f32(r):
                 for p in pre:
                     chk(qmm.qmm_matmul(synth.Q4_K, p["W"][r], p["M"], p["K"], p["X"], PREFILL_N, p["Y32"], p["ws"],
                                        stream=stream))
-            ops["prefill_f32"], launches_per_pass["prefill_f32"] = op_prefill_f32, 2 * len(pre)
+            ops["prefill_f32"] = op_prefill_f32
     allgather = None
     if args.allgather and world > 1 and "decode" in only:
         # the row slices of every decode output, gathered on every rank
@@ -335,8 +338,14 @@ def run_gpu(args):
     # one over the first K % R copies, so that exactly K steps are timed.
     K_steps = max(1, args.steps)
     full, rem = divmod(K_steps, R)
-    graphs = {name: (Timer(torch, stream, f, R), Timer(torch, stream, f, rem) if rem else None)
+    graphs = {name: (Timer(torch, stream, f, R, qmm.qmm_kernel_launches), Timer(torch, stream, f, rem) if rem else None)
               for name, f in ops.items()}
+    # launches per pass as the library counted them while the graphs were recorded
+    for name in graphs:
+        n = graphs[name][0].launches
+        if n != int(n) or n < 1:
+            raise RuntimeError(f"{name}: {n} library launches per pass")
+        launches_per_pass[name] = int(n)
     torch.cuda.synchronize()
     warm_replays = max(1, -(-max(args.warmup, 3) // R))
     for _ in range(warm_replays):

@@ -9,6 +9,15 @@
 #include "../../include/qmm.h"
 #include "kernels.h"
 
+namespace qmm {
+std::atomic<uint64_t> g_launches{0};
+
+cudaError_t launched(cudaError_t e) {
+    if (e == cudaSuccess) g_launches.fetch_add(1);
+    return e;
+}
+}  // namespace qmm
+
 namespace {
 
 using namespace qmm;
@@ -123,6 +132,7 @@ struct Settings {
     int gemv_max_n;   // QMM_GEMV_MAX_N: largest N qmm_matmul sends to the GEMV
     int force;        // QMM_FORCE_PATH: 0 none, 1 gemv, 2 gemm
     int gemm_bn;      // QMM_GEMM_BN: 0 = model-based choice
+    int gemm_ks;      // QMM_GEMM_KS: K split of the GEMM (1, 2, 4); 0 = by tile count
     int gemv_rows;    // QMM_GEMV_ROWS: 64, 128 or 256 rows per GEMV tile; 0 = by M
     int gemv_rg;      // QMM_GEMV_RG: 16-row groups per warp (1 or 2) of the resident-X GEMV
     int gemv_ks;      // QMM_GEMV_KS: K split of the GEMV (1..8); 0 = automatic
@@ -143,6 +153,8 @@ const Settings &settings() {
         t.force = (f && !std::strcmp(f, "gemv")) ? 1 : (f && !std::strcmp(f, "gemm")) ? 2 : 0;
         t.gemm_bn = env_int("QMM_GEMM_BN", 0);
         if (t.gemm_bn != 64 && t.gemm_bn != 128 && t.gemm_bn != 256) t.gemm_bn = 0;
+        t.gemm_ks = env_int("QMM_GEMM_KS", 0);
+        if (t.gemm_ks != 1 && t.gemm_ks != 2 && t.gemm_ks != 4) t.gemm_ks = 0;
         t.gemv_rows = env_int("QMM_GEMV_ROWS", 0);
         if (t.gemv_rows != 64 && t.gemv_rows != 128 && t.gemv_rows != 256) t.gemv_rows = 0;
         t.gemv_rg = env_int("QMM_GEMV_RG", 0) == 2 ? 2 : 1;
@@ -189,24 +201,72 @@ qmm_status validate(int wt, const void *W, size_t w_bytes, int64_t M, int64_t K,
 
 qmm_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QMM_OK : QMM_ERR_CUDA; }
 
-int choose_bn(int64_t M, int64_t N, int num_sms) {
-    const int forced = settings().gemm_bn;
-    if (forced) return forced;
-    // A tile's 64-k stage costs about max(~1100 cycles of fixed pipeline
-    // latency, 4 * BN cycles of MMA and X traffic); pick the BN with the
-    // fewest (waves x stage cost), the larger grid on a tie.
-    const int64_t tiles_m = (M + 127) / 128;
-    int best = 64;
-    double best_cost = 1e30;
+// Resident clusters of ks CTAs for (fmt, bn), per device (queried once).
+int cluster_capacity(int fmt, int bn, int ks, int num_sms) {
+    if (ks == 1) return num_sms;
+    static std::atomic<int> cache[8][5][3][3];   // device, format, bn, ks; 0 = not queried
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 8 || fmt < 0 || fmt > 4) return num_sms / ks;
+    const int bi = bn == 64 ? 0 : (bn == 128 ? 1 : 2), ki = ks == 2 ? 1 : 2;
+    int v = cache[dev][fmt][bi][ki].load();
+    if (v == 0) {
+        v = gemm_max_clusters(fmt, bn, ks);
+        if (v <= 0) v = -1;
+        cache[dev][fmt][bi][ki].store(v);
+    }
+    return v > 0 ? v : num_sms / ks / 2;
+}
+
+// Token tile BN and K split KS of the GEMM, and how the 128-row tiles are
+// divided between at most two launches.  A CTA spends about the same time on
+// a 256-k chunk whatever BN is (weight copy, dequantization and MMA overlap),
+// plus about two chunks' worth of set-up, drain and epilogue.  With fewer
+// tiles than a wave, a K split over a cluster (2 or 4 CTAs) shortens each
+// CTA's K range, as long as the split grid still fits one wave.  With more
+// tiles than a wave, the whole waves run unsplit and the tiles of the last,
+// partial wave run as a second launch, split when that is quicker.  Among
+// the BNs, the fewest estimated chunk-times wins; on a tie the larger BN
+// (less repeated dequantization).
+struct TilePlan {
+    int bn;
+    int mt_a, ks_a;   // first launch: m-tiles 0 .. mt_a - 1, K split ks_a
+    int ks_b;         // second launch (the remaining m-tiles, if any), K split ks_b
+    double cost;
+};
+
+TilePlan plan_tiles(int fmt, int64_t total_mt, int64_t N, int64_t K, int num_sms) {
+    const Settings &cfg = settings();
+    const int64_t nkc = K / 256;
+    TilePlan best{64, (int)total_mt, 1, 1, 1e30};
+    auto chunks = [&](int ks) { return (double)((nkc + ks - 1) / ks) + (ks > 1 ? 2.0 : 1.5); };
+    auto ks_ok = [&](int ks) {
+        if (cfg.gemm_ks) return ks == cfg.gemm_ks && ks <= nkc;
+        return ks == 1 || (nkc / ks >= 4);
+    };
     for (int bn : {256, 128, 64}) {
-        if (bn > 64 && N <= bn / 2) continue;   // a smaller tile covers N
-        const int64_t tiles = tiles_m * ((N + bn - 1) / bn);
-        const int64_t waves = (tiles + num_sms - 1) / num_sms;
-        const double stage = bn * 4.0 > 1100.0 ? bn * 4.0 : 1100.0;
-        const double cost = (double)waves * stage;
-        if (cost <= best_cost) {
-            best_cost = cost;
-            best = bn;
+        if (cfg.gemm_bn ? bn != cfg.gemm_bn : (bn > 64 && N <= bn / 2)) continue;   // a smaller tile covers N
+        const int64_t tn = (N + bn - 1) / bn, tiles = total_mt * tn;
+        // one launch, split within one wave or unsplit
+        for (int ks : {1, 2, 4}) {
+            if (!ks_ok(ks)) continue;
+            const int64_t cap = cluster_capacity(fmt, bn, ks, num_sms);
+            if (cap < 1 || (ks > 1 && tiles > cap)) continue;
+            const double cost = (double)((tiles + cap - 1) / cap) * chunks(ks);
+            if (cost < best.cost - 1e-9) best = TilePlan{bn, (int)total_mt, ks, ks, cost};
+        }
+        // whole waves unsplit, then the last wave's tiles split
+        if (!cfg.gemm_ks && tiles > num_sms && tiles % num_sms) {
+            const int64_t mt_a = tiles / num_sms * num_sms / tn;
+            const int64_t tail = (total_mt - mt_a) * tn;
+            if (mt_a < 1 || mt_a >= total_mt) continue;
+            const double head = (double)((mt_a * tn + num_sms - 1) / num_sms) * chunks(1);
+            for (int ks : {2, 4}) {
+                if (!ks_ok(ks)) continue;
+                const int64_t cap = cluster_capacity(fmt, bn, ks, num_sms);
+                if (cap < 1 || tail > cap) continue;
+                const double cost = head + chunks(ks);
+                if (cost < best.cost - 1e-9) best = TilePlan{bn, (int)mt_a, 1, ks, cost};
+            }
         }
     }
     return best;
@@ -424,7 +484,9 @@ qmm_status gemm_impl(int wt, const void *W, size_t w_bytes, int64_t M, int64_t K
         if (e != cudaSuccess) return QMM_ERR_CUDA;
         xb = workspace;
     }
-    const int bn = choose_bn(W2 ? 2 * M : M, N, di.num_sms);
+    const int64_t total_mt = (M + 127) / 128 * (W2 ? 2 : 1);
+    const TilePlan plan = plan_tiles(wt, total_mt, N, K, di.num_sms);
+    const int bn = plan.bn;
 
     CUtensorMap wmap, wmap2, xmap;
     for (int i = 0; i < (W2 ? 2 : 1); ++i) {
@@ -461,7 +523,17 @@ qmm_status gemm_impl(int wt, const void *W, size_t w_bytes, int64_t M, int64_t K
     a.status = di.status;
     a.wait_limit = g_wait_limit.load();
     a.pdl = static_weights() ? 1 : 0;
-    return from_cuda(launch_gemm_tc(a, wmap, wmap2, xmap, st));
+    a.ks = plan.ks_a;
+    a.mt0 = 0;
+    a.mtn = plan.mt_a;
+    cudaError_t e = launch_gemm_tc(a, wmap, wmap2, xmap, st);
+    if (e == cudaSuccess && plan.mt_a < total_mt) {
+        a.ks = plan.ks_b;
+        a.mt0 = plan.mt_a;
+        a.mtn = (int)(total_mt - plan.mt_a);
+        e = launch_gemm_tc(a, wmap, wmap2, xmap, st);
+    }
+    return from_cuda(e);
 }
 
 }  // namespace
@@ -587,6 +659,8 @@ qmm_status qmm_dequant(qmm_wtype wt, const void *W, size_t w_bytes, int64_t M, i
     if (overlaps(out, (size_t)M * K * 4, W, need)) return QMM_ERR_INVALID_ARG;
     return from_cuda(launch_dequant(wt, static_cast<const uint8_t *>(W), M, K, out, static_cast<cudaStream_t>(stream)));
 }
+
+uint64_t qmm_kernel_launches(void) { return qmm::g_launches.load(); }
 
 qmm_status qmm_last_device_error(void *stream) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -76,6 +76,8 @@ template <int F, int BN> struct Layout {
     static constexpr int TOTAL = OFF_MISC + 64;
     static constexpr int SMEM = TOTAL + 1024;     // 1024-byte alignment slack
     static_assert(SMEM <= 232448, "shared memory budget");
+    // K split: the slice partials (BM x BN f32) reuse the X and raw areas
+    static_assert(BM * BN * 4 <= OFF_BAR, "split-K partials fit below the barriers");
 };
 
 struct Ctl {
@@ -95,6 +97,20 @@ __device__ __forceinline__ bool wait_ok(const Ctl &c, uint64_t *bar, uint32_t pa
             return false;
         }
     }
+}
+
+// Cluster-wide barrier (every thread of every CTA of the cluster arrives).
+__device__ __forceinline__ void cluster_sync_epi() { cluster_sync_all(); }
+
+// 16 bytes of CTA `rank`'s shared memory at the offset of `local`.
+__device__ __forceinline__ float4 ld_dsmem_f32x4(const float4 *local, uint32_t rank) {
+    const uint32_t ra = cluster_addr(local, rank);
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(ra)
+                 : "memory");
+    return v;
 }
 
 // Drain wait: used after an abort for copies this thread issued itself;
@@ -234,7 +250,7 @@ __device__ __forceinline__ void dequant32<Q6_K>(const uint8_t *rb, int sub, int 
 template <int F, int BN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap wmap2,
-                   const __grid_constant__ CUtensorMap xmap, int M, int K, int N, float *__restrict__ Y1,
+                   const __grid_constant__ CUtensorMap xmap, int M, int K, int N, int mt0, float *__restrict__ Y1,
                    float *__restrict__ Y2, unsigned *status, uint64_t wait_limit) {
     using L = Layout<F, BN>;
     constexpr int SA = L::SA, SX = L::SX;
@@ -259,17 +275,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // share X, e.g. gate and up), the second half of the grid's x range
     // takes it.
     const int tiles_m = (M + BM - 1) / BM;
-    const bool second = Y2 != nullptr && (int)blockIdx.x >= tiles_m;
+    const int mt = mt0 + (int)blockIdx.x;   // this CTA's 128-row tile
+    const bool second = Y2 != nullptr && mt >= tiles_m;
     const CUtensorMap *wm = second ? &wmap2 : &wmap;
     float *__restrict__ Y = second ? Y2 : Y1;
-    const int m0 = (second ? (int)blockIdx.x - tiles_m : (int)blockIdx.x) * BM, n0 = blockIdx.y * BN;
-    const int nkc = K / KC;
+    const int m0 = (second ? mt - tiles_m : mt) * BM, n0 = blockIdx.y * BN;
+    // K split: the KS CTAs of a (1, 1, KS) cluster take slices of the chunks;
+    // rank 0 adds the other slices' partial sums (distributed shared memory,
+    // rank order) in the epilogue.
+    const int KS = (int)gridDim.z, zr = (int)blockIdx.z;
+    const int nkc_all = K / KC;
+    const int kc0 = nkc_all * zr / KS, nkc = nkc_all * (zr + 1) / KS - kc0;
     const int nsteps = nkc * (KC / BK);
-    // Each CTA walks K starting at its own chunk (a rotation): CTAs that run
-    // in lockstep then read different X tiles at any moment instead of all
-    // hitting the same L2 lines at once.  The k-sum is the same set of terms.
+    // Each CTA walks its chunks starting at its own offset (a rotation): CTAs
+    // that run in lockstep then read different X tiles at any moment instead
+    // of all hitting the same L2 lines at once.  The k-sum is the same set of
+    // terms.
     const int koff = (int)(((unsigned)(m0 / BM) * 5u + blockIdx.y * 3u) % (unsigned)nkc);
-    auto kchunk = [&](int c) { return c + koff < nkc ? c + koff : c + koff - nkc; };
+    auto kchunk = [&](int c) { return kc0 + (c + koff < nkc ? c + koff : c + koff - nkc); };
     const Ctl ctl{abort_flag, wait_limit};
     const uint64_t drain_limit = wait_limit < (1ull << 31) ? (1ull << 31) : wait_limit;
 
@@ -425,16 +448,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const bool acc_ok = mbar_wait(acc_full, 0, 2 * drain_limit);
         pdl_wait();   // Y: order after the preceding kernel
         tc_fence_after();
-        if (__all_sync(0xffffffffu, acc_ok && !*abort_flag)) {
-            const int q = warp & 3;                      // TMEM lanes 32q .. 32q+31
-            const int chalf = (warp - WARP_DQ0) >> 2;    // two warps per lane quarter split the columns
-            const int row = m0 + 32 * q + lane;
+        const bool good = __all_sync(0xffffffffu, acc_ok && !*abort_flag);
+        const int q = warp & 3;                      // TMEM lanes 32q .. 32q+31
+        const int chalf = (warp - WARP_DQ0) >> 2;    // two warps per lane quarter split the columns
+        const int rl = 32 * q + lane, row = m0 + rl;
+        // K split: slice partials in shared memory [column / 4][row][4] (the
+        // X stage area is free once every MMA has completed)
+        float4 *red = reinterpret_cast<float4 *>(sX);
+        if (good && (KS == 1 || zr != 0)) {
 #pragma unroll 1
             for (int j = chalf * (BN / 32); j < (chalf + 1) * (BN / 32); ++j) {
                 uint32_t v[16];
                 tmem_ld_32x32b_x16(tmem_d + ((uint32_t)(32 * q) << 16) + 16 * j, v);
                 tmem_ld_wait();
-                if (row < M) {
+                if (KS > 1) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        red[(4 * j + i) * BM + rl] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                                                 __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+                } else if (row < M) {
 #pragma unroll
                     for (int cidx = 0; cidx < 16; ++cidx) {
                         const int n = n0 + 16 * j + cidx;
@@ -443,6 +475,45 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
         }
+        if (KS > 1) {
+            // every CTA of the cluster reaches both barriers, aborted or not
+            cluster_sync_epi();
+            if (zr == 0 && good) {
+#pragma unroll 1
+                for (int j = chalf * (BN / 32); j < (chalf + 1) * (BN / 32); ++j) {
+                    uint32_t v[16];
+                    tmem_ld_32x32b_x16(tmem_d + ((uint32_t)(32 * q) << 16) + 16 * j, v);
+                    tmem_ld_wait();
+                    float acc[16];
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) acc[c] = __uint_as_float(v[c]);
+                    for (int r = 1; r < KS; ++r) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float4 p = ld_dsmem_f32x4(&red[(4 * j + i) * BM + rl], (uint32_t)r);
+                            acc[4 * i] += p.x;
+                            acc[4 * i + 1] += p.y;
+                            acc[4 * i + 2] += p.z;
+                            acc[4 * i + 3] += p.w;
+                        }
+                    }
+                    if (row < M) {
+#pragma unroll
+                        for (int cidx = 0; cidx < 16; ++cidx) {
+                            const int n = n0 + 16 * j + cidx;
+                            if (n < N) Y[(int64_t)n * M + row] = acc[cidx];
+                        }
+                    }
+                }
+            }
+            cluster_sync_epi();   // rank 0 has read every partial: the others may exit
+        }
+    }
+    if (KS > 1 && warp < WARP_DQ0) {
+        // the other warps take part in the epilogue's cluster barriers
+        __syncwarp();
+        cluster_sync_epi();
+        cluster_sync_epi();
     }
 
     tc_fence_before();
@@ -470,13 +541,20 @@ cudaError_t launch_one(const GemmArgs &a, const CUtensorMap &wmap, const CUtenso
         configured.fetch_or(bit);
     }
     cudaLaunchConfig_t cfg = {};
-    const int64_t tiles_m = (a.M + BM - 1) / BM;
-    cfg.gridDim = dim3((unsigned)(tiles_m * (a.Y2 ? 2 : 1)), (unsigned)((a.N + BN - 1) / BN), 1);
+    cfg.gridDim = dim3((unsigned)a.mtn, (unsigned)((a.N + BN - 1) / BN), 1);
     cfg.blockDim = dim3(NUM_THREADS, 1, 1);
     cfg.dynamicSmemBytes = L::SMEM;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cfg.gridDim.z = (unsigned)a.ks;
+    cudaLaunchAttribute attr[2];
     unsigned na = 0;
+    if (a.ks > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = 1;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = (unsigned)a.ks;
+        ++na;
+    }
     if (a.pdl) {
         attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[na].val.programmaticStreamSerializationAllowed = 1;
@@ -484,10 +562,10 @@ cudaError_t launch_one(const GemmArgs &a, const CUtensorMap &wmap, const CUtenso
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    e = cudaLaunchKernelEx(&cfg, kern, wmap, wmap2, xmap, (int)a.M, (int)a.K, a.N, a.Y, a.Y2, a.status,
+    e = cudaLaunchKernelEx(&cfg, kern, wmap, wmap2, xmap, (int)a.M, (int)a.K, a.N, a.mt0, a.Y, a.Y2, a.status,
                            a.wait_limit);
     if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    return launched(cudaGetLastError());
 }
 
 template <int F>
@@ -504,6 +582,52 @@ cudaError_t launch_fmt(const GemmArgs &a, const CUtensorMap &wmap, const CUtenso
 }  // namespace
 
 int gemm_x_stages_per_copy(int) { return 1; }
+
+namespace {
+template <int F, int BN>
+int cluster_slots_one(int ks) {
+    using L = Layout<F, BN>;
+    auto kern = gemm_tc_kernel<F, BN>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM) != cudaSuccess) return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, 1, (unsigned)ks);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = L::SMEM;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = (unsigned)ks;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+template <int F>
+int cluster_slots_fmt(int bn, int ks) {
+    switch (bn) {
+    case 64: return cluster_slots_one<F, 64>(ks);
+    case 128: return cluster_slots_one<F, 128>(ks);
+    case 256: return cluster_slots_one<F, 256>(ks);
+    default: return 0;
+    }
+}
+}   // namespace
+
+int gemm_max_clusters(int fmt, int bn, int ks) {
+    switch (fmt) {
+    case Q8_0: return cluster_slots_fmt<Q8_0>(bn, ks);
+    case Q4_0: return cluster_slots_fmt<Q4_0>(bn, ks);
+    case Q4_K: return cluster_slots_fmt<Q4_K>(bn, ks);
+    case Q6_K: return cluster_slots_fmt<Q6_K>(bn, ks);
+    case Q5_K: return cluster_slots_fmt<Q5_K>(bn, ks);
+    default: return 0;
+    }
+}
 
 int gemm_raw_window_bytes(int fmt) {
     switch (fmt) {

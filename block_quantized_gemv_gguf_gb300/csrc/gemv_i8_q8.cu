@@ -102,7 +102,7 @@ cudaError_t launch_quant(const void *X, int xbf16, int64_t count, float *scales,
         e = xbf16 ? cudaLaunchKernelEx(&cfg, quantize_q8_0_kernel<true, false>, X, nblocks, scales, quants, o)
                   : cudaLaunchKernelEx(&cfg, quantize_q8_0_kernel<false, false>, X, nblocks, scales, quants, o);
     if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    return launched(cudaGetLastError());
 }
 }  // namespace
 

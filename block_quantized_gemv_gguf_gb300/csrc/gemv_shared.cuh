@@ -251,7 +251,7 @@ cudaError_t launch_cluster(Kern kern, int smem, int threads, int64_t tiles, int 
     const cudaError_t e =
         cudaLaunchKernelEx(&cfg, kern, segs, x_arg, (int)K, N, cps, status, limit, amax);
     if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    return launched(cudaGetLastError());
 }
 
 template <typename Kern>

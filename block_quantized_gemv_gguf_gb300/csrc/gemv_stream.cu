@@ -556,7 +556,7 @@ cudaError_t launch_typed(const StreamPlan &p, const StreamArgs &a, bool pdl, cud
     cfg.numAttrs = pdl ? 1 : 0;
     e = cudaLaunchKernelEx(&cfg, kern, a);
     if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    return launched(cudaGetLastError());
 }
 
 template <int F>

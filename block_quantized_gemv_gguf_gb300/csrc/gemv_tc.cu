@@ -768,7 +768,7 @@ cudaError_t tc_launch_typed(const TcPlan &p, const CUtensorMap &wmap, const TcAr
     cfg.numAttrs = pdl ? 1 : 0;
     e = cudaLaunchKernelEx(&cfg, kern, wmap, a);
     if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    return launched(cudaGetLastError());
 }
 
 template <int F>

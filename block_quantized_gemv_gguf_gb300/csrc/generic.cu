@@ -120,7 +120,7 @@ cudaError_t launch_dequant(int fmt, const uint8_t *W, int64_t M, int64_t K, floa
     case Q5_K: dequant_kernel<Q5_K><<<g, 256, 0, st>>>(W, M, K, out); break;
     default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
+    return launched(cudaGetLastError());
 }
 
 template <int F>
@@ -143,7 +143,7 @@ cudaError_t launch_gemv_generic(int fmt, const uint8_t *W, int64_t M, int64_t K,
     case Q5_K: gemv_generic_dispatch<Q5_K>(W, M, K, X, xbf16, N, Y, st); break;
     default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
+    return launched(cudaGetLastError());
 }
 
 cudaError_t launch_x_to_bf16(const float *X, int64_t count, uint16_t *out, bool pdl, cudaStream_t st) {
@@ -159,7 +159,7 @@ cudaError_t launch_x_to_bf16(const float *X, int64_t count, uint16_t *out, bool 
     cfg.numAttrs = pdl ? 1 : 0;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, x_to_bf16_kernel, X, count, reinterpret_cast<__nv_bfloat16 *>(out));
     if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    return launched(cudaGetLastError());
 }
 
 }  // namespace qmm
@@ -179,7 +179,7 @@ cudaError_t launch_swiglu(const float *g, const float *u, int64_t count, float *
     cfg.numAttrs = pdl ? 1 : 0;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, swiglu_kernel, g, u, count, out);
     if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    return launched(cudaGetLastError());
 }
 
 }  // namespace qmm

@@ -7,6 +7,10 @@
 
 namespace qmm {
 
+// Counts e == cudaSuccess as one kernel launch and returns e (every launch
+// site of the library returns through it).
+cudaError_t launched(cudaError_t e);
+
 // out[M,K] = dequantized W (f32, one rounding of the exact value).
 cudaError_t launch_dequant(int fmt, const uint8_t *W, int64_t M, int64_t K, float *out, cudaStream_t st);
 
@@ -151,6 +155,9 @@ struct GemmArgs {
     int bn;          // token tile (64, 128 or 256)
     float *Y;
     float *Y2;       // second matrix's output (wmap2; same M and K), or null
+    int ks;          // K split over a (1, 1, ks) cluster: 1, 2 or 4 (ks <= K / 256)
+    int mt0, mtn;    // this launch's 128-row tiles: mt0 .. mt0 + mtn - 1 (with Y2, the
+                     // second matrix's tiles follow the first's)
     unsigned *status;
     uint64_t wait_limit;
     int pdl;         // programmatic dependent launch (weights read before the preceding kernel ends)
@@ -161,6 +168,9 @@ cudaError_t launch_gemm_tc(const GemmArgs &a, const CUtensorMap &wmap, const CUt
                            const CUtensorMap &xmap, cudaStream_t st);
 
 int gemm_x_stages_per_copy(int bn);
+// Clusters of ks CTAs (1, 2, 4) of the GEMM kernel for (fmt, bn) that can be
+// resident at once on the current device (0 if the query fails).
+int gemm_max_clusters(int fmt, int bn, int ks);
 
 // Window of raw weight bytes one 256-weight chunk of a row occupies in the
 // GEMM's shared-memory staging (bytes; a multiple of 16).

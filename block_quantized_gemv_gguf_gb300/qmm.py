@@ -30,7 +30,8 @@ EXPORTS = ("qmm_gemv", "qmm_gemv_argmax", "qmm_gemv_multi", "qmm_gemm", "qmm_gem
            "qmm_dequant", "qmm_block_info", "qmm_last_device_error", "qmm_status_str",
            "qmm_set_wait_limit", "qmm_set_static_weights", "qmm_set_gemv_i8", "qmm_set_gemv_tc", "qmm_quantize_q8_0",
            "qmm_gemv_preq", "qmm_q8act_workspace_bytes", "qmm_gemv_q8act", "qmm_gemv_swiglu",
-           "qmm_gemm_q8act_workspace_bytes", "qmm_gemm_q8act", "qmm_gemm_swiglu_workspace_bytes", "qmm_gemm_swiglu")
+           "qmm_gemm_q8act_workspace_bytes", "qmm_gemm_q8act", "qmm_gemm_swiglu_workspace_bytes", "qmm_gemm_swiglu",
+           "qmm_kernel_launches")
 
 _lock = threading.Lock()
 _lib = None
@@ -89,6 +90,8 @@ def load() -> ctypes.CDLL:
         lib.qmm_gemm_swiglu_workspace_bytes.argtypes = [i64, i64, i64, ci]
         lib.qmm_gemm_swiglu_workspace_bytes.restype = sz
         lib.qmm_gemm_swiglu.argtypes = [ci, p, sz, p, sz, i64, i64, p, ci, i64, p, p, sz, p]
+        lib.qmm_kernel_launches.argtypes = []
+        lib.qmm_kernel_launches.restype = ctypes.c_uint64
         for f in ("qmm_gemv", "qmm_gemv_argmax", "qmm_gemv_multi", "qmm_gemm", "qmm_matmul", "qmm_matmul_host", "qmm_dequant", "qmm_block_info",
                   "qmm_last_device_error", "qmm_quantize_q8_0", "qmm_gemv_preq", "qmm_gemv_q8act", "qmm_gemv_swiglu",
                   "qmm_gemm_q8act", "qmm_gemm_swiglu"):
@@ -210,6 +213,10 @@ def qmm_block_info(wt):
 
 def qmm_gemm_workspace_bytes(N, K, xt) -> int:
     return load().qmm_gemm_workspace_bytes(N, K, xt)
+
+
+def qmm_kernel_launches() -> int:
+    return int(load().qmm_kernel_launches())
 
 
 def qmm_last_device_error(stream=None) -> int:

@@ -266,6 +266,16 @@ QMM_API qmm_status qmm_last_device_error(void *stream);
 QMM_API const char *qmm_status_str(qmm_status s);
 
 /*
+ * Number of kernels this library has launched in this process so far, across
+ * all devices and streams: each successful launch counts once, including a
+ * launch recorded into a CUDA graph under stream capture (a graph replay
+ * launches nothing through the library and is not counted).  Callers take
+ * the difference over a region, e.g. the capture of one pass of their work,
+ * to learn how many kernels that work runs.  Never fails.
+ */
+QMM_API uint64_t qmm_kernel_launches(void);
+
+/*
  * Static-weights mode, process wide, for launches issued after the call
  * (default off; the environment variable QMM_STATIC_WEIGHTS=1 turns it on
  * until this function is first called).  On: the tensor-core GEMV and GEMM

@@ -76,8 +76,11 @@ import numpy as np, torch, oracle
 from block_quantized_gemv_gguf_gb300 import qmm, synth
 qmm.load()
 bad = []
-for wt in (synth.Q4_0, synth.Q4_K, synth.Q6_K, synth.Q8_0):
-    for (M, K, N) in ((300, 2048, 100), (128, 2048, 17), (520, 4096, 512)):
+for wt in (synth.Q4_0, synth.Q4_K, synth.Q6_K, synth.Q8_0, synth.Q5_K):
+    for (M, K, N) in ((300, 2048, 100), (128, 2048, 17), (520, 4096, 512), (200, 2304, 40), (130, 256, 20)):
+        E, B = synth.BLOCK[wt]
+        if (K // E * B) % 16:
+            continue   # rows not 16-byte multiples: the GEMM does not take them
         w = synth.gen_weights(wt, M, K, "tune-gemm")
         W = torch.from_numpy(w).cuda()
         x = synth.gen_x(N, K, "tune-gemm")
@@ -100,13 +103,18 @@ GEMM_COMBOS = [
     {"QMM_GEMM_BN": "64"},
     {"QMM_GEMM_BN": "128"},
     {"QMM_GEMM_BN": "256"},
+    {"QMM_GEMM_KS": "1"},
+    {"QMM_GEMM_KS": "2", "QMM_GEMM_BN": "256"},
+    {"QMM_GEMM_KS": "4", "QMM_GEMM_BN": "64"},
+    {"QMM_GEMM_KS": "4", "QMM_GEMM_BN": "128"},
 ]
 
 
 @pytest.mark.parametrize("env", GEMM_COMBOS, ids=lambda e: "-".join(f"{k[9:].lower()}{v}" for k, v in e.items()))
 def test_forced_gemm_shapes(env):
     """The tensor-core GEMM with every token tile (M not a multiple of the
-    128-row tile: the partial tiles must stay inside Y)."""
+    128-row tile: the partial tiles must stay inside Y) and every K split
+    (K = 2304 splits its 9 chunks 4/5 and 2/2/2/3; K = 256 cannot split)."""
     import torch
     if not torch.cuda.is_available():
         pytest.skip("needs a GPU")
