@@ -508,6 +508,7 @@ int unit_bytes_of(int fmt) {
 }
 
 constexpr int kSmemMax = 232448 - 1024;   // the opt-in maximum, less room for static shared words
+constexpr int kSmemPerSM = 233472;        // shared memory of one SM (two CTAs: each also has 1 KB reserved)
 
 // Shared-memory layout for nw warps, S slots, K and up to nst stages.
 struct StreamLayout {
@@ -570,15 +571,25 @@ bool plan_gemv_stream(int fmt, int64_t M, int64_t K, int num_sms, int force_warp
     const int ub = unit_bytes_of(fmt);
     if (!ub || K % 256 || M < 1 || num_sms < 1 || K > (1 << 15)) return false;
     if ((K / 256 * ub) % 16) return false;   // rows must start 16-byte aligned
-    int64_t grid = M < num_sms ? M : num_sms;
+    // Short launches (K <= 4096, at most 64 MB of weights) run two CTAs of
+    // at most 8 warps per SM: when one launch follows another on the stream,
+    // the next launch's CTAs then start (and stream their weights) on SMs
+    // where the previous launch's CTAs are still finishing.  Measured on
+    // Q4_0 / Q8_0 / Q4_K rows of 4096: 5-6% shorter launches; long rows
+    // (every CTA stages all of X) and long launches do better with one.
+    const int64_t wbytes = M * (K / 256) * ub;
+    int cps = K <= 4096 && wbytes <= (64ll << 20) ? 2 : 1;
+    if (force_warps > 16 / cps) cps = 1;
+    const int lim = cps == 2 ? kSmemPerSM / 2 - 3072 : kSmemMax;
+    int64_t grid = M < (int64_t)cps * num_sms ? M : (int64_t)cps * num_sms;
     for (int attempt = 0; attempt < 8; ++attempt) {
         const int64_t rows = (M + grid - 1) / grid;
         const int64_t nst = (rows * (K / 256) + kLanes - 1) / kLanes;
         for (int nw : {16, 12, 8, 4}) {
-            if (force_warps && nw != force_warps) continue;
+            if (force_warps ? nw != force_warps : nw > 16 / cps) continue;
             for (int S : {3, 2}) {
                 const StreamLayout L = stream_layout(fmt, nw, S, K, nst);
-                if (L.total <= kSmemMax) {
+                if (L.total <= lim) {
                     p.grid = (int)grid;
                     p.warps = nw;
                     p.S = S;
