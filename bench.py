@@ -611,7 +611,7 @@ def run_crossover(torch, qmm, stream, dev, args, chk):
     Ws = [{name: torch.from_numpy(synth.gen_weights(wt, M, K, f"layer{c}.{name}")).to(dev)
            for name, wt, M, K in synth.DECODER_LAYER} for c in range(R)]
     rows = []
-    for N in (2, 4, 8, 12, 16, 24, 32):
+    for N in (2, 4, 6, 8, 9, 10, 11, 12, 16, 24, 32):
         X = {K: torch.from_numpy(synth.gen_x(N, K, f"xover-{N}-{K}")).to(dev) for K in (4096, 14336)}
         Ys = {name: torch.empty(N, M, device=dev) for name, _, M, _ in synth.DECODER_LAYER}
         ws = torch.empty(max(qmm.qmm_gemm_workspace_bytes(N, 14336, qmm.X_F32), 16), dtype=torch.uint8, device=dev)

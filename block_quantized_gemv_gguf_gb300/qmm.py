@@ -24,7 +24,7 @@ Q8_0, Q4_0, Q4_K, Q6_K, Q5_K = 0, 1, 2, 3, 4
 X_F32, X_BF16 = 0, 1
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = 0, 1, 2, 3, 4
 GEMV_MAX_N, GEMM_MAX_N = 16, 512
-MATMUL_GEMV_MAX_N = 15   # qmm_matmul's default GEMV/GEMM crossover (QMM_MATMUL_GEMV_MAX_N)
+MATMUL_GEMV_MAX_N = 8    # qmm_matmul's default GEMV/GEMM crossover (QMM_MATMUL_GEMV_MAX_N)
 BLOCK = {Q8_0: (32, 34), Q4_0: (32, 18), Q4_K: (256, 144), Q6_K: (256, 210), Q5_K: (256, 176)}
 EXPORTS = ("qmm_gemv", "qmm_gemv_argmax", "qmm_gemv_multi", "qmm_gemm", "qmm_gemm_workspace_bytes", "qmm_matmul", "qmm_matmul_host",
            "qmm_dequant", "qmm_block_info", "qmm_last_device_error", "qmm_status_str",

@@ -95,10 +95,11 @@ typedef enum {
 #define QMM_GEMV_MAX_N 16
 #define QMM_GEMM_MAX_N 512
 /* Largest N qmm_matmul sends to the GEMV by default (the environment
- * variable QMM_GEMV_MAX_N can lower it): measured on GB300 over the seven
- * projections of one decoder layer, the GEMV is faster up to N = 12 and the
- * GEMM is as fast from N = 16. */
-#define QMM_MATMUL_GEMV_MAX_N 15
+ * variable QMM_GEMV_MAX_N can change it): measured on GB300 over the seven
+ * projections of one decoder layer (Q4_K/Q6_K, CUDA graphs), the GEMV takes
+ * 95-131 us for N = 2..8 and 216-281 us for N = 9..16, the K-split GEMM
+ * 135-141 us for every N from 2 to 32. */
+#define QMM_MATMUL_GEMV_MAX_N 8
 
 /*
  * Multi-token GEMV, 1 <= N <= QMM_GEMV_MAX_N: decode (N = 1) and small-N
