@@ -75,7 +75,13 @@ def peaks():
 # capture each (dram__bytes_read.sum + dram__bytes_write.sum), keyed by the
 # sha256 of the kernel sources they were taken on: any source change since
 # the capture turns the figure into null.
-TRAFFIC = {}
+TRAFFIC = {
+    # kernel sources 1acd349a8980132f; profiles/launch_list_bench_step.md
+    "decode": ("1acd349a8980132f", 78_113_000),       # 4 launches of the streaming GEMV
+    "lmhead": ("1acd349a8980132f", 452_251_000),      # ring GEMV, Q6_K 128256x4096, N=8
+    "prefill": ("1acd349a8980132f", 55_165_000),      # 3 GEMM launches (bf16 X)
+    "prefill_f32": ("1acd349a8980132f", 71_958_000),  # 2 conversions + 3 GEMM launches
+}
 
 
 def _kernel_hash():
