@@ -70,6 +70,22 @@ __device__ __forceinline__ float2 dot4(float2 acc, uint32_t v, float2 off, float
     return __ffma2_rn(__fadd2_rn(mag23(v), off), f2(x.z, x.w), acc);
 }
 
+// Offset-free codes (Q4_K, Q5_K: q in 0..31) as exact f32 subnormals: a byte
+// permute puts the code alone into the low byte, so the f32 reads
+// q * 2^-149 with no constant to remove.  X is stored scaled per 32-element
+// block by 2^k (k from the block's largest |x|, below), so the products
+// q * x * 2^(k - 149) are normal numbers; the block sum is scaled back by
+// 2^64 * 2^(85 - k) (two exact power-of-two multiplies).
+__device__ __forceinline__ float sub_code(uint32_t w, uint32_t k) {
+    return __uint_as_float(__byte_perm(w, 0u, 0x4440u | k));
+}
+// acc += codes of bytes 0..3 of v (as subnormals) * x[0..3]
+__device__ __forceinline__ float2 dot4s(float2 acc, uint32_t v, float4 x) {
+    acc = __ffma2_rn(f2(sub_code(v, 0), sub_code(v, 1)), f2(x.x, x.y), acc);
+    return __ffma2_rn(f2(sub_code(v, 2), sub_code(v, 3)), f2(x.z, x.w), acc);
+}
+__device__ __forceinline__ float unscale(float v, float fb) { return (v * 0x1p64f) * fb; }
+
 // The unit's 64 chunks of x, XOR-swizzled: logical chunk 8k + t sits at
 // p[t][8k] (the XOR only touches t, so k is an immediate offset).
 struct XRow {
@@ -111,13 +127,13 @@ __device__ __forceinline__ void lds_words(uint32_t (&r)[NW], const uint8_t *p) {
 // of the unit (Q4_K / Q5_K).
 // ---------------------------------------------------------------------------
 template <int F>
-__device__ __forceinline__ float unit_dot(const uint8_t *ub, const XRow &x, const float *xs8);
+__device__ __forceinline__ float unit_dot(const uint8_t *ub, const XRow &x, const float *xs8, const float *fb8);
 
 // Q4_0: 8 blocks; block b at byte 18b: f16 d, 16 bytes qs; element e < 16
 // is the low nibble of qs[e], e >= 16 the high nibble of qs[e - 16];
 // w = (nibble - 8) * d.
 template <>
-__device__ __forceinline__ float unit_dot<Q4_0>(const uint8_t *ub, const XRow &x, const float *) {
+__device__ __forceinline__ float unit_dot<Q4_0>(const uint8_t *ub, const XRow &x, const float *, const float *) {
     uint32_t r[36];
     lds_words(r, ub);
     const float2 off = f2(-8388616.f, -8388616.f);   // -(2^23 + 8)
@@ -141,7 +157,7 @@ __device__ __forceinline__ float unit_dot<Q4_0>(const uint8_t *ub, const XRow &x
 // code byte with its sign bit flipped is q + 128.  Each half (4 blocks) is
 // read separately to bound the registers.
 template <>
-__device__ __forceinline__ float unit_dot<Q8_0>(const uint8_t *ub, const XRow &x, const float *) {
+__device__ __forceinline__ float unit_dot<Q8_0>(const uint8_t *ub, const XRow &x, const float *, const float *) {
     const float2 off = f2(-8388736.f, -8388736.f);   // -(2^23 + 128)
     float y = 0.f;
 #pragma unroll
@@ -187,15 +203,19 @@ __device__ __forceinline__ void kq_header(uint32_t r0, uint32_t w0, uint32_t w1,
 // Q4_K: d @0, dmin @2, scales @4..15, qs @16..143; element e = 32 s + l is
 // the low (s even) or high (s odd) nibble of qs[32 (s / 2) + l];
 // w = d sc_s q - dmin m_s, summed as dsc_s * sum(q x) - dmn_s * sum(x).
+// sum(q x) from subnormal codes and the block-scaled x (fb8: the unit's 8
+// scale-back factors), sum(x) from the f32 sums of the unscaled x (xs8).
 template <>
-__device__ __forceinline__ float unit_dot<Q4_K>(const uint8_t *ub, const XRow &x, const float *xs8) {
+__device__ __forceinline__ float unit_dot<Q4_K>(const uint8_t *ub, const XRow &x, const float *xs8,
+                                                const float *fb8) {
     uint32_t r[36];
     lds_words(r, ub);
     float dsc[8], dmn[8];
     kq_header(r[0], r[1], r[2], r[3], dsc, dmn);
     const float4 xa = *reinterpret_cast<const float4 *>(xs8), xb = *reinterpret_cast<const float4 *>(xs8 + 4);
     const float xsum[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
-    const float2 off = f2(-8388608.f, -8388608.f);
+    const float4 fa = *reinterpret_cast<const float4 *>(fb8), fc = *reinterpret_cast<const float4 *>(fb8 + 4);
+    const float fb[8] = {fa.x, fa.y, fa.z, fa.w, fc.x, fc.y, fc.z, fc.w};
     float y = 0.f;
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
@@ -203,12 +223,12 @@ __device__ __forceinline__ float unit_dot<Q4_K>(const uint8_t *ub, const XRow &x
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
             const uint32_t w = r[4 + 8 * p + t];
-            alo = dot4(alo, w & 0x0F0F0F0Fu, off, x(16 * p + t));
-            ahi = dot4(ahi, (w >> 4) & 0x0F0F0F0Fu, off, x(16 * p + 8 + t));
+            alo = dot4s(alo, w & 0x0F0F0F0Fu, x(16 * p + t));
+            ahi = dot4s(ahi, (w >> 4) & 0x0F0F0F0Fu, x(16 * p + 8 + t));
         }
-        y = fmaf(dsc[2 * p], alo.x + alo.y, y);
+        y = fmaf(dsc[2 * p], unscale(alo.x + alo.y, fb[2 * p]), y);
         y = fmaf(-dmn[2 * p], xsum[2 * p], y);
-        y = fmaf(dsc[2 * p + 1], ahi.x + ahi.y, y);
+        y = fmaf(dsc[2 * p + 1], unscale(ahi.x + ahi.y, fb[2 * p + 1]), y);
         y = fmaf(-dmn[2 * p + 1], xsum[2 * p + 1], y);
     }
     return y;
@@ -217,14 +237,16 @@ __device__ __forceinline__ float unit_dot<Q4_K>(const uint8_t *ub, const XRow &x
 // Q5_K: as Q4_K with qh[32] @16 and qs @48; bit s of qh[l] is bit 4 of
 // element 32 s + l.
 template <>
-__device__ __forceinline__ float unit_dot<Q5_K>(const uint8_t *ub, const XRow &x, const float *xs8) {
+__device__ __forceinline__ float unit_dot<Q5_K>(const uint8_t *ub, const XRow &x, const float *xs8,
+                                                const float *fb8) {
     uint32_t r[44];
     lds_words(r, ub);
     float dsc[8], dmn[8];
     kq_header(r[0], r[1], r[2], r[3], dsc, dmn);
     const float4 xa = *reinterpret_cast<const float4 *>(xs8), xb = *reinterpret_cast<const float4 *>(xs8 + 4);
     const float xsum[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
-    const float2 off = f2(-8388608.f, -8388608.f);
+    const float4 fa = *reinterpret_cast<const float4 *>(fb8), fc = *reinterpret_cast<const float4 *>(fb8 + 4);
+    const float fb[8] = {fa.x, fa.y, fa.z, fa.w, fc.x, fc.y, fc.z, fc.w};
     float y = 0.f;
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
@@ -234,12 +256,12 @@ __device__ __forceinline__ float unit_dot<Q5_K>(const uint8_t *ub, const XRow &x
             const uint32_t w = r[12 + 8 * p + t], qh = r[4 + t];
             const uint32_t qlo = (w & 0x0F0F0F0Fu) | (((qh >> (2 * p)) & 0x01010101u) << 4);
             const uint32_t qhi = ((w >> 4) & 0x0F0F0F0Fu) | (((qh >> (2 * p + 1)) & 0x01010101u) << 4);
-            alo = dot4(alo, qlo, off, x(16 * p + t));
-            ahi = dot4(ahi, qhi, off, x(16 * p + 8 + t));
+            alo = dot4s(alo, qlo, x(16 * p + t));
+            ahi = dot4s(ahi, qhi, x(16 * p + 8 + t));
         }
-        y = fmaf(dsc[2 * p], alo.x + alo.y, y);
+        y = fmaf(dsc[2 * p], unscale(alo.x + alo.y, fb[2 * p]), y);
         y = fmaf(-dmn[2 * p], xsum[2 * p], y);
-        y = fmaf(dsc[2 * p + 1], ahi.x + ahi.y, y);
+        y = fmaf(dsc[2 * p + 1], unscale(ahi.x + ahi.y, fb[2 * p + 1]), y);
         y = fmaf(-dmn[2 * p + 1], xsum[2 * p + 1], y);
     }
     return y;
@@ -251,7 +273,7 @@ __device__ __forceinline__ float unit_dot<Q5_K>(const uint8_t *ub, const XRow &x
 // qh[32 h + l]; w = d * scales[e / 16] * (q - 32).  The unit starts at an
 // even byte; words are assembled from 4-byte aligned loads.
 template <>
-__device__ __forceinline__ float unit_dot<Q6_K>(const uint8_t *ub, const XRow &x, const float *) {
+__device__ __forceinline__ float unit_dot<Q6_K>(const uint8_t *ub, const XRow &x, const float *, const float *) {
     const uint32_t sh = (uint32_t)(reinterpret_cast<uintptr_t>(ub) & 2u) * 8u;   // 0 or 16 bits
     const uint32_t *wp = reinterpret_cast<const uint32_t *>(ub - (sh >> 3));
     auto W = [&](int i) { return __funnelshift_r(wp[i], wp[i + 1], sh); };
@@ -384,7 +406,12 @@ __global__ void __launch_bounds__(512, 1) gemv_stream_kernel(const __grid_consta
 
     pdl_wait();   // X and Y are ordered behind the preceding grid
 
-    // X -> shared memory, f32, chunk (p, q) of 4 floats at p * 64 + (q ^ (p & 7))
+    // X -> shared memory, f32, chunk (p, q) of 4 floats at p * 64 + (q ^ (p & 7)).
+    // Q4_K / Q5_K: each 32-element block (8 consecutive chunks, 8 consecutive
+    // threads: K / 4 is a multiple of 64, so every warp runs every round)
+    // is stored times 2^k, k = 126 - E clamped to [-1, 127] (E: the binary
+    // exponent of the block's largest |x|), with its scale-back factor
+    // 2^(85 - k) and the f32 sum of its unscaled elements.
     {
         float4 *xs4 = reinterpret_cast<float4 *>(xs);
         const int nch = a.K >> 2;
@@ -397,22 +424,28 @@ __global__ void __launch_bounds__(512, 1) gemv_stream_kernel(const __grid_consta
             } else {
                 v = reinterpret_cast<const float4 *>(a.X)[c];
             }
+            if constexpr (kmin_fmt(F)) {
+                float m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+                float sx = (v.x + v.y) + (v.z + v.w);
+#pragma unroll
+                for (int o = 1; o < 8; o <<= 1) {
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                    sx += __shfl_xor_sync(0xffffffffu, sx, o);
+                }
+                int k = 126 - ((int)(__float_as_uint(m) >> 23) - 127);
+                k = k < -1 ? -1 : (k > 127 ? 127 : k);
+                const float sc = __uint_as_float((uint32_t)(127 + k) << 23);   // 2^k
+                v.x *= sc;
+                v.y *= sc;
+                v.z *= sc;
+                v.w *= sc;
+                if ((c & 7) == 0) {
+                    xsum[c >> 3] = sx;
+                    xsum[(a.K >> 5) + (c >> 3)] = __uint_as_float((uint32_t)(212 - k) << 23);   // 2^(85 - k)
+                }
+            }
             const int p = c >> 6, q = c & 63;
             xs4[(p << 6) | (q ^ (p & 7))] = v;
-        }
-    }
-    if constexpr (kmin_fmt(F)) {
-        __syncthreads();
-        const float4 *xs4 = reinterpret_cast<const float4 *>(xs);
-        for (int i = threadIdx.x; i < (a.K >> 5); i += blockDim.x) {   // sub-block i = 8 p + s
-            const int p = i >> 3, s = i & 7;
-            float acc = 0.f;
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const float4 v = xs4[(p << 6) | ((8 * s + c) ^ (p & 7))];
-                acc += (v.x + v.y) + (v.z + v.w);
-            }
-            xsum[i] = acc;
         }
     }
     __syncthreads();
@@ -433,7 +466,7 @@ __global__ void __launch_bounds__(512, 1) gemv_stream_kernel(const __grid_consta
             key = u / U;                   // row of the unit (within the CTA)
             const int p = u - key * U;     // unit within the row
             const XRow xr(xs4 + (p << 6), p & 7);
-            v = unit_dot<F>(sm + (size_t)slot * SLOT + lane * UB, xr, xsum + 8 * p);
+            v = unit_dot<F>(sm + (size_t)slot * SLOT + lane * UB, xr, xsum + 8 * p, xsum + (a.K >> 5) + 8 * p);
         }
         __syncwarp();
         if (lane == 0 && j + S < my_nst) issue(j + S);   // every lane has read the slot
@@ -521,7 +554,7 @@ StreamLayout stream_layout(int fmt, int nw, int S, int64_t K, int64_t nst) {
     L.off_x = (int)o;
     o += K * 4;
     L.off_xsum = (int)o;
-    o += kmin_fmt(fmt) ? K / 8 : 0;
+    o += kmin_fmt(fmt) ? K / 4 : 0;   // per 32-element block: the sum of x, then the scale-back factor
     o = (o + 15) / 16 * 16;
     L.off_part = (int)o;
     o += (nst * 8 + 15) / 16 * 16;

@@ -99,6 +99,44 @@ def test_gemm_swiglu_matches_oracle(wt, M, K, N, xbf16):
     assert oracle.within(u, Yu, Su, *GEMM_TOL)[0]
 
 
+@pytest.mark.parametrize("wt", [synth.Q4_K, synth.Q8_0], ids=["Q4_K", "Q8_0"])
+def test_gemm_swiglu_two_launch_plan(wt):
+    """More 128-row tiles (both matrices) than one wave holds: whole waves run
+    unsplit and the last tiles (the second matrix's) run as a second,
+    K-split launch; every row checked against the oracle."""
+    M, K, N = 5000, 2048, 300
+    wg = synth.gen_weights(wt, M, K, "gemm-gate-big")
+    wu = synth.gen_weights(wt, M, K, "gemm-up-big")
+    x, X = _x(N, K, "gemm-swiglu-big", True)
+    n = qmm.load().qmm_gemm_swiglu_workspace_bytes(N, M, K, qmm.X_BF16)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    Y = qmm.gemm_swiglu(wt, torch.from_numpy(wg).cuda(), torch.from_numpy(wu).cuda(), M, K, X, workspace=ws)
+    torch.cuda.synchronize()
+    Yg, Sg = oracle.matmul(wt, wg, M, K, x)
+    Yu, Su = oracle.matmul(wt, wu, M, K, x)
+    out, bound = oracle.swiglu(Yg, Sg, Yu, Su, *GEMM_TOL)
+    err = np.abs(Y.cpu().numpy().astype(np.float64) - out)
+    assert np.all(err <= bound), f"worst err/bound {np.max(err / bound):.3g}"
+
+
+@pytest.mark.parametrize("wt", [synth.Q4_K, synth.Q8_0, synth.Q6_K], ids=["Q4_K", "Q8_0", "Q6_K"])
+def test_gemm_two_launch_plan_ragged_rows(wt):
+    """155 row tiles (the last one partial) at N = 100: a wave of 152 tiles,
+    then 3 tiles split over clusters; sampled rows, the last tiles in full."""
+    M, K, N = 152 * 128 + 300, 2048, 100
+    w = synth.gen_weights(wt, M, K, "gemm-two-launch")
+    x, X = _x(N, K, "gemm-two-launch", False)
+    Y = torch.full((N, M), float("nan"), device="cuda")
+    assert qmm.qmm_gemm(wt, torch.from_numpy(w).cuda(), M, K, X, N, Y, qmm.workspace_for(N, K, X)) == qmm.OK
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(5)
+    rows = np.sort(np.concatenate([rng.choice(152 * 128, 256, replace=False), np.arange(152 * 128, M)]))
+    Yr, S = oracle.matmul(wt, w, M, K, x, rows=rows)
+    ok, ratio = oracle.within(Y.cpu().numpy()[:, rows], Yr, S, *GEMM_TOL)
+    assert ok, f"worst |err|/tol = {ratio:.3g}"
+    assert torch.all(torch.isfinite(Y))
+
+
 def test_invalid_arguments_write_nothing():
     wt, M, K, N = synth.Q4_K, 256, 2048, 64
     W = torch.from_numpy(synth.gen_weights(wt, M, K, "bad")).cuda()
