@@ -76,11 +76,11 @@ def peaks():
 # sha256 of the kernel sources they were taken on: any source change since
 # the capture turns the figure into null.
 TRAFFIC = {
-    # kernel sources 1acd349a8980132f; profiles/launch_list_bench_step.md
-    "decode": ("1acd349a8980132f", 78_113_000),       # 4 launches of the streaming GEMV
-    "lmhead": ("1acd349a8980132f", 452_251_000),      # ring GEMV, Q6_K 128256x4096, N=8
-    "prefill": ("1acd349a8980132f", 55_165_000),      # 3 GEMM launches (bf16 X)
-    "prefill_f32": ("1acd349a8980132f", 71_958_000),  # 2 conversions + 3 GEMM launches
+    # kernel sources 2899f3b7b1b947c2: the launch list of `bench.py --steps 8 --copies 2 --no-extras` under ncu
+    "decode": ("2899f3b7b1b947c2", 78_104_000),       # 4 launches of the streaming GEMV
+    "lmhead": ("2899f3b7b1b947c2", 452_300_000),      # ring GEMV, Q6_K 128256x4096, N=8
+    "prefill": ("2899f3b7b1b947c2", 55_146_000),      # 3 GEMM launches (bf16 X)
+    "prefill_f32": ("2899f3b7b1b947c2", 71_935_000),  # 2 conversions + 3 GEMM launches
 }
 
 
