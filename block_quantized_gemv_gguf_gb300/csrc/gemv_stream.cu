@@ -412,40 +412,55 @@ __global__ void __launch_bounds__(512, 1) gemv_stream_kernel(const __grid_consta
     // is stored times 2^k, k = 126 - E clamped to [-1, 127] (E: the binary
     // exponent of the block's largest |x|), with its scale-back factor
     // 2^(85 - k) and the f32 sum of its unscaled elements.
+    // The loads of a batch of XB chunks per thread are all issued before any
+    // is used, so that staging costs about one L2 round trip per batch.
     {
         float4 *xs4 = reinterpret_cast<float4 *>(xs);
         const int nch = a.K >> 2;
-        for (int c = threadIdx.x; c < nch; c += blockDim.x) {
-            float4 v;
-            if constexpr (XBF16) {
-                const uint2 b = reinterpret_cast<const uint2 *>(a.X)[c];
-                v = make_float4(__uint_as_float(b.x << 16), __uint_as_float(b.x & 0xFFFF0000u),
-                                __uint_as_float(b.y << 16), __uint_as_float(b.y & 0xFFFF0000u));
-            } else {
-                v = reinterpret_cast<const float4 *>(a.X)[c];
-            }
-            if constexpr (kmin_fmt(F)) {
-                float m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
-                float sx = (v.x + v.y) + (v.z + v.w);
+        constexpr int XB = 8;
+        for (int c0 = threadIdx.x; c0 < nch; c0 += XB * blockDim.x) {
+            float4 vb[XB];
 #pragma unroll
-                for (int o = 1; o < 8; o <<= 1) {
-                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-                    sx += __shfl_xor_sync(0xffffffffu, sx, o);
-                }
-                int k = 126 - ((int)(__float_as_uint(m) >> 23) - 127);
-                k = k < -1 ? -1 : (k > 127 ? 127 : k);
-                const float sc = __uint_as_float((uint32_t)(127 + k) << 23);   // 2^k
-                v.x *= sc;
-                v.y *= sc;
-                v.z *= sc;
-                v.w *= sc;
-                if ((c & 7) == 0) {
-                    xsum[c >> 3] = sx;
-                    xsum[(a.K >> 5) + (c >> 3)] = __uint_as_float((uint32_t)(212 - k) << 23);   // 2^(85 - k)
+            for (int i = 0; i < XB; ++i) {
+                const int c = c0 + i * (int)blockDim.x;
+                if (c < nch) {
+                    if constexpr (XBF16) {
+                        const uint2 b = reinterpret_cast<const uint2 *>(a.X)[c];
+                        vb[i] = make_float4(__uint_as_float(b.x << 16), __uint_as_float(b.x & 0xFFFF0000u),
+                                            __uint_as_float(b.y << 16), __uint_as_float(b.y & 0xFFFF0000u));
+                    } else {
+                        vb[i] = reinterpret_cast<const float4 *>(a.X)[c];
+                    }
                 }
             }
-            const int p = c >> 6, q = c & 63;
-            xs4[(p << 6) | (q ^ (p & 7))] = v;
+#pragma unroll
+            for (int i = 0; i < XB; ++i) {
+                const int c = c0 + i * (int)blockDim.x;
+                if (c >= nch) break;   // warp-uniform: nch is a multiple of 64
+                float4 v = vb[i];
+                if constexpr (kmin_fmt(F)) {
+                    float m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+                    float sx = (v.x + v.y) + (v.z + v.w);
+#pragma unroll
+                    for (int o = 1; o < 8; o <<= 1) {
+                        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                        sx += __shfl_xor_sync(0xffffffffu, sx, o);
+                    }
+                    int k = 126 - ((int)(__float_as_uint(m) >> 23) - 127);
+                    k = k < -1 ? -1 : (k > 127 ? 127 : k);
+                    const float sc = __uint_as_float((uint32_t)(127 + k) << 23);   // 2^k
+                    v.x *= sc;
+                    v.y *= sc;
+                    v.z *= sc;
+                    v.w *= sc;
+                    if ((c & 7) == 0) {
+                        xsum[c >> 3] = sx;
+                        xsum[(a.K >> 5) + (c >> 3)] = __uint_as_float((uint32_t)(212 - k) << 23);   // 2^(85 - k)
+                    }
+                }
+                const int p = c >> 6, q = c & 63;
+                xs4[(p << 6) | (q ^ (p & 7))] = v;
+            }
         }
     }
     __syncthreads();
