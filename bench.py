@@ -603,10 +603,97 @@ def run_workloads(torch, qmm, stream, dev, args, chk):
                                     "frac_of_measured_hbm": round(b / (t * 1e-3) / 1e9 / hbm_peak, 4)}
     del w
 
+    out["next_rows"] = run_next_rows(torch, qmm, dev, R, chk, timed)
+
     if not args.no_sweep:
         out["decoder_sweep"] = run_sweep(torch, qmm, stream, dev, args, chk)
         out["gemv_gemm_crossover"] = run_crossover(torch, qmm, stream, dev, args, chk)
     return out
+
+
+def run_next_rows(torch, qmm, dev, R, chk, timed):
+    """The fused and alternative entry points against their unfused or
+    default counterparts, timed the same way (graphs over R rotating weight
+    copies; the LM head is one copy, larger than L2)."""
+    def us(t):
+        return round(t * 1e3, 3)
+
+    def copies(wt, M, K, name):
+        w = torch.from_numpy(synth.gen_weights(wt, M, K, name)).to(dev)
+        return [w] + [w.clone() for _ in range(R - 1)]
+
+    res = {}
+    K = 4096
+    x1 = torch.from_numpy(synth.gen_x(1, K, "next-x1")).to(dev)
+
+    # F2: Q/K/V (Q4_K 4096 + 1024 + 1024 rows), N = 1, one launch vs three
+    qkv = [(copies(synth.Q4_K, M, K, f"next-{n}"), M) for n, M in (("q", 4096), ("k", 1024), ("v", 1024))]
+    Ys = [torch.empty(1, M, device=dev) for _, M in qkv]
+    fused = timed(lambda r: chk(qmm.qmm_gemv_multi(synth.Q4_K, [(W[r], M, Y) for (W, M), Y in zip(qkv, Ys)], K, x1, 1,
+                                                   stream=torch.cuda.current_stream())), R)
+    sep = timed(lambda r: [chk(qmm.qmm_gemv(synth.Q4_K, W[r], M, K, x1, 1, Y, stream=torch.cuda.current_stream()))
+                           for (W, M), Y in zip(qkv, Ys)], R)
+    res["f2_qkv_gemv_q4_k_n1"] = {"fused_us": us(fused), "three_calls_us": us(sep)}
+    del qkv
+
+    # F2: gate/up + SwiGLU (Q4_K 2 x 14336 rows), N = 1 and N = 512
+    M = 14336
+    g, u = copies(synth.Q4_K, M, K, "next-gate"), copies(synth.Q4_K, M, K, "next-up")
+    Y1 = torch.empty(1, M, device=dev)
+    ws1 = torch.empty(2 * M, dtype=torch.float32, device=dev)
+    Yg, Yu = torch.empty(1, M, device=dev), torch.empty(1, M, device=dev)
+    fused = timed(lambda r: chk(qmm.qmm_gemv_swiglu(synth.Q4_K, g[r], u[r], M, K, x1, 1, Y1, ws1,
+                                                    stream=torch.cuda.current_stream())), R)
+    sep = timed(lambda r: (chk(qmm.qmm_gemv(synth.Q4_K, g[r], M, K, x1, 1, Yg, stream=torch.cuda.current_stream())),
+                           chk(qmm.qmm_gemv(synth.Q4_K, u[r], M, K, x1, 1, Yu, stream=torch.cuda.current_stream()))), R)
+    res["f2_gate_up_swiglu_gemv_q4_k_n1"] = {"fused_us": us(fused), "two_gemvs_us": us(sep)}
+    N = 512
+    xb = torch.from_numpy(synth.f32_to_bf16_bits(synth.gen_x(N, K, "next-x512"))).to(dev).view(torch.bfloat16)
+    Yn = torch.empty(N, M, device=dev)
+    wsn = torch.empty(qmm.load().qmm_gemm_swiglu_workspace_bytes(N, M, K, qmm.X_BF16), dtype=torch.uint8, device=dev)
+    Ygn, Yun = torch.empty(N, M, device=dev), torch.empty(N, M, device=dev)
+    fused = timed(lambda r: chk(qmm.qmm_gemm_swiglu(synth.Q4_K, g[r], u[r], M, K, xb, N, Yn, wsn,
+                                                    stream=torch.cuda.current_stream())), R)
+    sep = timed(lambda r: (chk(qmm.qmm_gemm(synth.Q4_K, g[r], M, K, xb, N, Ygn, stream=torch.cuda.current_stream())),
+                           chk(qmm.qmm_gemm(synth.Q4_K, u[r], M, K, xb, N, Yun, stream=torch.cuda.current_stream()))), R)
+    fl = 2 * 2.0 * M * K * N
+    res["f2_gate_up_swiglu_gemm_q4_k_n512"] = {"fused_us": us(fused), "two_gemms_us": us(sep),
+                                               "fused_TFLOPs": round(fl / (fused * 1e-3) / 1e12, 1)}
+    del u
+
+    # F4: Q8_0 activations, GEMV at N = 8 and GEMM at N = 512, against the default paths
+    x8 = torch.from_numpy(synth.gen_x(8, K, "next-x8")).to(dev)
+    Y8 = torch.empty(8, M, device=dev)
+    ws8 = torch.empty(qmm.qmm_q8act_workspace_bytes(8, K), dtype=torch.uint8, device=dev)
+    q8 = timed(lambda r: chk(qmm.qmm_gemv_q8act(synth.Q4_K, g[r], M, K, x8, 8, Y8, ws8,
+                                                stream=torch.cuda.current_stream())), R)
+    dflt = timed(lambda r: chk(qmm.qmm_gemv(synth.Q4_K, g[r], M, K, x8, 8, Y8, stream=torch.cuda.current_stream())), R)
+    res["f4_q8act_gemv_q4_k_14336x4096_n8"] = {"q8act_us": us(q8), "f32_gemv_us": us(dflt)}
+    x512 = torch.from_numpy(synth.gen_x(N, K, "next-x512")).to(dev)
+    wsq = torch.empty(qmm.load().qmm_gemm_q8act_workspace_bytes(N, K), dtype=torch.uint8, device=dev)
+    wsf = qmm.workspace_for(N, K, x512)
+    q8 = timed(lambda r: chk(qmm.qmm_gemm_q8act(synth.Q4_K, g[r], M, K, x512, N, Yn, wsq,
+                                                stream=torch.cuda.current_stream())), R)
+    dflt = timed(lambda r: chk(qmm.qmm_gemm(synth.Q4_K, g[r], M, K, x512, N, Yn, wsf,
+                                            stream=torch.cuda.current_stream())), R)
+    res["f4_q8act_gemm_q4_k_14336x4096_n512"] = {"q8act_us": us(q8), "f32_gemm_us": us(dflt)}
+    del g
+
+    # F3: argmax-fused LM head (Q6_K 128256 x 4096), N = 1
+    Mh, Kh, _ = LMHEAD
+    w = torch.from_numpy(synth.gen_weights(synth.Q6_K, Mh, Kh, "bench-lmhead")).to(dev)
+    xh = torch.from_numpy(synth.gen_x(1, Kh, "next-xh")).to(dev)
+    idx = torch.empty(1, dtype=torch.int32, device=dev)
+    val = torch.empty(1, dtype=torch.float32, device=dev)
+    wsa = torch.empty(2, dtype=torch.int64, device=dev)
+    Yh = torch.empty(1, Mh, device=dev)
+    am = timed(lambda r: chk(qmm.qmm_gemv_argmax(synth.Q6_K, w, Mh, Kh, xh, 1, idx, val, wsa,
+                                                 stream=torch.cuda.current_stream())), 1, reps=10)
+    gv = timed(lambda r: chk(qmm.qmm_gemv(synth.Q6_K, w, Mh, Kh, xh, 1, Yh, stream=torch.cuda.current_stream())), 1,
+               reps=10)
+    res["f3_argmax_lmhead_q6_k_n1"] = {"argmax_us": us(am), "gemv_us": us(gv),
+                                       "note": "the GEMV also writes 513 KB of logits that the argmax path never stores"}
+    return res
 
 
 def run_crossover(torch, qmm, stream, dev, args, chk):

@@ -94,14 +94,25 @@ __global__ void x_to_bf16_kernel(const float *__restrict__ X, int64_t count, __n
 // src/backend/cpu.rs", silu_mul_inplace: the SwiGLU product of the gate and
 // up projections).  exp overflows to infinity for v < -88, where the
 // quotient is -0: the exact value is below 1e-36 * |v|.
+__device__ __forceinline__ float silu_mul(float v, float w) { return v / (1.0f + expf(-v)) * w; }
+
+// Grid-stride over 4-element groups (16-byte loads and stores when all three
+// arrays are 16-byte aligned), a few thousand CTAs at most: one element per
+// thread in a CTA per 256 elements made block scheduling the limit.
 __global__ void swiglu_kernel(const float *__restrict__ g, const float *__restrict__ u, int64_t count,
                               float *__restrict__ out) {
     pdl_launch_dependents();
     pdl_wait();   // g and u come from the preceding kernel
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < count; i += (int64_t)gridDim.x * blockDim.x) {
-        const float v = g[i];
-        out[i] = v / (1.0f + expf(-v)) * u[i];
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t t0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const bool vec = (((uintptr_t)g | (uintptr_t)u | (uintptr_t)out) & 15u) == 0;
+    const int64_t n4 = vec ? count / 4 : 0;
+    for (int64_t i = t0; i < n4; i += stride) {
+        const float4 a = reinterpret_cast<const float4 *>(g)[i], b = reinterpret_cast<const float4 *>(u)[i];
+        reinterpret_cast<float4 *>(out)[i] =
+            make_float4(silu_mul(a.x, b.x), silu_mul(a.y, b.y), silu_mul(a.z, b.z), silu_mul(a.w, b.w));
     }
+    for (int64_t i = 4 * n4 + t0; i < count; i += stride) out[i] = silu_mul(g[i], u[i]);
 }
 
 static int grid_for(int64_t work, int per_block) {
@@ -169,7 +180,10 @@ namespace qmm {
 cudaError_t launch_swiglu(const float *g, const float *u, int64_t count, float *out, bool pdl, cudaStream_t st) {
     if (count <= 0) return cudaSuccess;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid_for(count, 256), 1, 1);
+    const int64_t groups = (count + 3) / 4;
+    int64_t blocks = (groups + 255) / 256;
+    if (blocks > 2432) blocks = 2432;   // 16 per SM on 152 SMs
+    cfg.gridDim = dim3((unsigned)blocks, 1, 1);
     cfg.blockDim = dim3(256, 1, 1);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];

@@ -119,6 +119,33 @@ def test_gemm_swiglu_two_launch_plan(wt):
     assert np.all(err <= bound), f"worst err/bound {np.max(err / bound):.3g}"
 
 
+@pytest.mark.parametrize("xbf16", [False, True], ids=["f32x", "bf16x"])
+def test_gemm_swiglu_full_size(xbf16):
+    """Gate/up at 14336 x 4096, N = 300: 448 tiles of both matrices in one
+    paired plan (whole waves, then the rest).  Sampled rows (the last tile
+    in full) against the oracle, and g, u left in the workspace."""
+    wt, M, K, N = synth.Q4_K, 14336, 4096, 300
+    wg = synth.gen_weights(wt, M, K, "gemm-gate-sep")
+    wu = synth.gen_weights(wt, M, K, "gemm-up-sep")
+    x, X = _x(N, K, "gemm-swiglu-sep", xbf16)
+    xt = qmm.X_BF16 if xbf16 else qmm.X_F32
+    ws = torch.empty(qmm.load().qmm_gemm_swiglu_workspace_bytes(N, M, K, xt), dtype=torch.uint8, device="cuda")
+    Y = qmm.gemm_swiglu(wt, torch.from_numpy(wg).cuda(), torch.from_numpy(wu).cuda(), M, K, X, workspace=ws)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(11)
+    rows = np.sort(np.concatenate([rng.choice(M - 128, 192, replace=False), np.arange(M - 128, M)]))
+    Yg, Sg = oracle.matmul(wt, wg, M, K, x, rows=rows)
+    Yu, Su = oracle.matmul(wt, wu, M, K, x, rows=rows)
+    out, bound = oracle.swiglu(Yg, Sg, Yu, Su, *GEMM_TOL)
+    err = np.abs(Y.cpu().numpy()[:, rows].astype(np.float64) - out)
+    assert np.all(err <= bound), f"worst err/bound {np.max(err / bound):.3g}"
+    xws = (qmm.qmm_gemm_workspace_bytes(N, K, xt) + 15) // 16 * 16
+    g = ws[xws:xws + N * M * 4].view(torch.float32).view(N, M).cpu().numpy()[:, rows]
+    u = ws[xws + N * M * 4:xws + 2 * N * M * 4].view(torch.float32).view(N, M).cpu().numpy()[:, rows]
+    assert oracle.within(g, Yg, Sg, *GEMM_TOL)[0]
+    assert oracle.within(u, Yu, Su, *GEMM_TOL)[0]
+
+
 @pytest.mark.parametrize("wt", [synth.Q4_K, synth.Q8_0, synth.Q6_K], ids=["Q4_K", "Q8_0", "Q6_K"])
 def test_gemm_two_launch_plan_ragged_rows(wt):
     """155 row tiles (the last one partial) at N = 100: a wave of 152 tiles,
