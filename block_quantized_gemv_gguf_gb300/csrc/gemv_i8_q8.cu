@@ -82,8 +82,10 @@ cudaError_t launch_quant(const void *X, int xbf16, int64_t count, float *scales,
                          bool pdl, cudaStream_t st) {
     const int64_t nblocks = count / 32;
     if (nblocks <= 0) return cudaSuccess;
+    // grid-stride: at most 16 CTAs per SM of 152 (one 32-element block per
+    // warp and CTA pass; more, smaller CTAs made block scheduling the limit)
     int64_t grid = (nblocks + 7) / 8;
-    if (grid > (1 << 20)) grid = 1 << 20;
+    if (grid > 2432) grid = 2432;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
     cfg.blockDim = dim3(256, 1, 1);
