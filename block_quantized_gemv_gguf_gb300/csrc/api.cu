@@ -40,6 +40,9 @@ std::atomic<int> g_gemv_i8{-1};
 // 16-row-tile tensor-core GEMV for 2 <= N <= QMM_TC_MAX_N: -1 = not set
 // through the API, take QMM_GEMV_TC from the environment (default off).
 std::atomic<int> g_gemv_tc{-1};
+// Streaming GEMV plan parameters set through qmm_set_gemv_stream (rows per
+// task, warps, slots, CTAs per SM): -1 = not set, take the environment's.
+std::atomic<int> g_stream_force[4] = {-1, -1, -1, -1};
 bool gemv_i8_on() {
     const int v = g_gemv_i8.load();
     if (v >= 0) return v != 0;
@@ -138,7 +141,10 @@ struct Settings {
     int gemv_ks;      // QMM_GEMV_KS: K split of the GEMV (1..8); 0 = automatic
     int gemv_res;     // QMM_GEMV_RESIDENT: 0 disables the resident-X GEMV
     int stream;       // QMM_GEMV_STREAM: 0 disables the streaming N = 1 GEMV
-    int stream_warps; // QMM_STREAM_WARPS: warps per CTA of the streaming GEMV (0 = by shared memory)
+    int stream_warps; // QMM_STREAM_WARPS: warps per CTA of the streaming GEMV, 1..16 (0 = by shared memory)
+    int stream_r;     // QMM_STREAM_R: rows per task of the streaming GEMV, 1, 2 or 4 (0 = by shape)
+    int stream_slots; // QMM_STREAM_SLOTS: stage slots per warp, 1..3 (0 = by shared memory)
+    int stream_cps;   // QMM_STREAM_CPS: CTAs per SM, 1 or 2 (0 = by shape)
     int tc;           // QMM_GEMV_TC: 1 enables the 16-row-tile tensor-core GEMV (opt-in, see qmm_set_gemv_tc)
     int tc_warps;     // QMM_TC_WARPS: warps per CTA of that kernel (0 = by shared memory)
     int tc_max_n;     // QMM_TC_MAX_N: largest N it serves (default 4; above, the ring GEMV is faster)
@@ -163,8 +169,13 @@ const Settings &settings() {
         t.gemv_res = env_int("QMM_GEMV_RESIDENT", 1) != 0;
         t.stream = env_int("QMM_GEMV_STREAM", 1) != 0;
         t.stream_warps = env_int("QMM_STREAM_WARPS", 0);
-        if (t.stream_warps != 4 && t.stream_warps != 8 && t.stream_warps != 12 && t.stream_warps != 16)
-            t.stream_warps = 0;
+        if (t.stream_warps < 0 || t.stream_warps > 16) t.stream_warps = 0;
+        t.stream_r = env_int("QMM_STREAM_R", 0);
+        if (t.stream_r != 1 && t.stream_r != 2 && t.stream_r != 4) t.stream_r = 0;
+        t.stream_slots = env_int("QMM_STREAM_SLOTS", 0);
+        if (t.stream_slots < 0 || t.stream_slots > 3) t.stream_slots = 0;
+        t.stream_cps = env_int("QMM_STREAM_CPS", 0);
+        if (t.stream_cps != 1 && t.stream_cps != 2) t.stream_cps = 0;
         t.tc = env_int("QMM_GEMV_TC", 0) != 0;
         t.tc_warps = env_int("QMM_TC_WARPS", 0);
         if (t.tc_warps != 4 && t.tc_warps != 8 && t.tc_warps != 16) t.tc_warps = 0;
@@ -174,6 +185,17 @@ const Settings &settings() {
         return t;
     }();
     return s;
+}
+
+StreamForce stream_force() {
+    const Settings &t = settings();
+    const int env[4] = {t.stream_r, t.stream_warps, t.stream_slots, t.stream_cps};
+    int v[4];
+    for (int i = 0; i < 4; ++i) {
+        const int g = g_stream_force[i].load();
+        v[i] = g >= 0 ? g : env[i];
+    }
+    return StreamForce{v[0], v[1], v[2], v[3]};
 }
 
 // Common validation of W, M, K, X, N, Y.
@@ -343,7 +365,7 @@ qmm_status gemv_segments(int wt, const SegIn *seg, int nseg, int64_t K, const vo
     if (fast && nseg == 1 && N == 1 && !q8 && !want_i8 && settings().stream) {
         // one token: the streaming kernel, when the shape fits it
         StreamPlan sp{};
-        if (plan_gemv_stream(wt, seg[0].M, K, di.num_sms, settings().stream_warps, sp))
+        if (plan_gemv_stream(wt, seg[0].M, K, di.num_sms, stream_force(), sp))
             return from_cuda(launch_gemv_stream(wt, sp, static_cast<const uint8_t *>(seg[0].W), seg[0].M, K, X,
                                                 xt == QMM_X_BF16, seg[0].Y, !amax && static_weights(), di.status,
                                                 g_wait_limit.load(), st, amax, idx, val));
@@ -701,6 +723,27 @@ qmm_status qmm_gemv_swiglu(qmm_wtype wt, const void *Wg, size_t wg_bytes, const 
 void qmm_set_gemv_i8(int on) { g_gemv_i8.store(on < 0 ? -1 : (on ? 1 : 0)); }
 
 void qmm_set_gemv_tc(int on) { g_gemv_tc.store(on < 0 ? -1 : (on ? 1 : 0)); }
+
+void qmm_set_gemv_stream(int rows_per_task, int warps, int slots, int ctas_per_sm) {
+    const int v[4] = {rows_per_task, warps, slots, ctas_per_sm};
+    for (int i = 0; i < 4; ++i) g_stream_force[i].store(v[i] < 0 ? -1 : v[i]);
+}
+
+qmm_status qmm_gemv_stream_plan(qmm_wtype wt, int64_t M, int64_t K, int32_t *plan) {
+    if (!plan || M < 1 || K < 1) return QMM_ERR_INVALID_ARG;
+    int E = 0, B = 0;
+    if (!block_geom(wt, E, B)) return QMM_ERR_INVALID_ARG;
+    DevInfo di;
+    if (!dev_info(di)) return QMM_ERR_CUDA;
+    StreamPlan sp{};
+    if (!plan_gemv_stream(wt, M, K, di.num_sms, stream_force(), sp)) return QMM_ERR_UNSUPPORTED;
+    plan[0] = sp.grid;
+    plan[1] = sp.warps;
+    plan[2] = sp.S;
+    plan[3] = sp.R;
+    plan[4] = sp.smem;
+    return QMM_OK;
+}
 
 size_t qmm_q8act_workspace_bytes(int64_t N, int64_t K) {
     if (N < 1 || K < 1) return 0;

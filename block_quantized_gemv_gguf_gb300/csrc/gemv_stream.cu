@@ -6,31 +6,39 @@
 // the row loops of "cera 0.5.2 src/backend/cpu.rs" (matmul_*_f32 /
 // gemv_dispatch), restated for one GB300 SM per CTA:
 //
-//   * Work unit = 256 consecutive weights of one row (8 Q4_0 / Q8_0 blocks,
-//     or one Q4_K / Q5_K / Q6_K super-block): 144, 272, 176 or 210 bytes.
+//   * Unit = 256 consecutive weights of one row (8 Q4_0 / Q8_0 blocks, or
+//     one Q4_K / Q5_K / Q6_K super-block): 144, 272, 176 or 210 bytes.
 //     A CTA owns whole rows; its rows are one contiguous byte range of W.
-//   * Each warp streams its own "stages" of 32 consecutive units of that
-//     range (one 1-D bulk copy per stage, completion on a warp-private
-//     mbarrier, a ring of S slots).  Lane l of the warp owns unit l of the
-//     stage.  No data passes between warps until the very end.
+//   * Task = the units of R consecutive rows (a "row group") at one unit
+//     column p: the R units share the same 256 x values, which a lane reads
+//     from shared memory once and applies to all R rows.  With R = 4 the
+//     shared-memory traffic of X (4 bytes per weight at R = 1, against 0.56
+//     bytes of Q4_0 weights) drops four-fold.
+//   * Tasks are numbered group-major (t = g U + p, U units per row).  Each
+//     warp streams its own "stages" of 32 consecutive tasks: one bulk copy
+//     per (row, run of columns) piece of the stage -- a single copy when the
+//     stage is contiguous in W -- completing on a warp-private mbarrier, in a
+//     ring of S slots.  Lane l owns task l of the stage.  No data passes
+//     between warps until the very end.
 //   * The weight copies are issued before the kernel waits on the preceding
 //     grid (the weights are static; X and Y are ordered behind it).
 //   * X (f32; bf16 widened) sits in shared memory once per CTA, in 16-byte
-//     chunks XOR-swizzled by unit index so that the 32 lanes of a warp, each
-//     on its own unit, read it without bank conflicts.
+//     chunks XOR-swizzled by unit column so that the 32 lanes of a warp,
+//     each on its own column, read it without bank conflicts.
 //   * Arithmetic: every integer code becomes an exact f32 by a byte permute
 //     into the mantissa of 2^23 and one packed subtraction (which also
 //     removes the format's offset), then a packed f32 FMA with x.  Each
 //     block's (or sub-block's) scale multiplies the f32 block sum; the
 //     Q4_K / Q5_K min term uses the sub-block sums of x.
-//   * Row results: a segmented warp-shuffle reduction by row over each
-//     stage (a row held entirely in one stage is stored directly); rows that
-//     cross stages are summed from per-stage partials in stage order at the
-//     end.  Every sum has a fixed order: the result is deterministic.
+//   * Row results: a segmented warp-shuffle reduction by row group over each
+//     stage (a group held entirely in one stage is stored directly); groups
+//     that cross stages are summed from per-stage partials in stage order at
+//     the end.  Every sum has a fixed order: the result is deterministic.
 //
 // All waits are bounded; a warp that gives up raises the CTA's abort flag,
 // waits (bounded) for its own copies in flight, and the CTA reports
 // QMM_ERR_TIMEOUT in the status word.
+#include <algorithm>
 #include <atomic>
 
 #include "amax.cuh"
@@ -48,9 +56,9 @@ template <> struct UnitBytes<Q5_K> { static constexpr int B = 176; };
 template <> struct UnitBytes<Q6_K> { static constexpr int B = 210; };
 
 constexpr int kLanes = 32;
-// A stage slot: 32 units, padded (the Q6_K reader fetches up to 4 bytes past
-// its unit) and rounded to 128 bytes.
-__host__ __device__ constexpr int slot_bytes(int ub) { return (kLanes * ub + 16 + 127) / 128 * 128; }
+// A stage slot: 32 tasks of R units, padded (the Q6_K reader fetches up to
+// 4 bytes past its unit) and rounded to 128 bytes.
+__host__ __device__ constexpr int slot_bytes(int ub, int R) { return (kLanes * R * ub + 16 + 127) / 128 * 128; }
 
 // ---------------------------------------------------------------------------
 // Exact integer codes as f32: a byte permute puts a code byte into the
@@ -86,8 +94,8 @@ __device__ __forceinline__ float2 dot4s(float2 acc, uint32_t v, float4 x) {
 }
 __device__ __forceinline__ float unscale(float v, float fb) { return (v * 0x1p64f) * fb; }
 
-// The unit's 64 chunks of x, XOR-swizzled: logical chunk 8k + t sits at
-// p[t][8k] (the XOR only touches t, so k is an immediate offset).
+// The unit column's 64 chunks of x, XOR-swizzled: logical chunk 8k + t sits
+// at p[t][8k] (the XOR only touches t, so k is an immediate offset).
 struct XRow {
     const float4 *p[8];
     __device__ __forceinline__ XRow(const float4 *x0, int sw) {
@@ -98,7 +106,7 @@ struct XRow {
 };
 
 // 32-bit word at byte offset `o` (even, compile-time after unrolling) of a
-// register copy of 16-byte aligned bytes.
+// register copy of 4-byte aligned bytes.
 template <int NW>
 __device__ __forceinline__ uint32_t word_at(const uint32_t (&r)[NW], int o) {
     return (o & 2) ? __byte_perm(r[o >> 2], r[(o >> 2) + 1], 0x5432u) : r[o >> 2];
@@ -108,8 +116,20 @@ __device__ __forceinline__ uint32_t half_at(const uint32_t (&r)[NW], int o) {
     return (o & 2) ? (r[o >> 2] >> 16) : (r[o >> 2] & 0xFFFFu);
 }
 
+// NW words from an 8-byte aligned shared-memory address.
 template <int NW>
-__device__ __forceinline__ void lds_words(uint32_t (&r)[NW], const uint8_t *p) {
+__device__ __forceinline__ void lds_w64(uint32_t (&r)[NW], const uint8_t *p) {
+    const uint2 *q = reinterpret_cast<const uint2 *>(p);
+#pragma unroll
+    for (int i = 0; i < NW / 2; ++i) {
+        const uint2 v = q[i];
+        r[2 * i] = v.x;
+        r[2 * i + 1] = v.y;
+    }
+}
+// NW words from a 16-byte aligned shared-memory address.
+template <int NW>
+__device__ __forceinline__ void lds_w128(uint32_t (&r)[NW], const uint8_t *p) {
     const uint4 *q = reinterpret_cast<const uint4 *>(p);
 #pragma unroll
     for (int i = 0; i < NW / 4; ++i) {
@@ -122,200 +142,282 @@ __device__ __forceinline__ void lds_words(uint32_t (&r)[NW], const uint8_t *p) {
 }
 
 // ---------------------------------------------------------------------------
-// One unit: sum over its 256 weights of w * x.  ub: the unit's bytes in
-// shared memory; x: the unit's 64 x chunks; xs8: the 8 sub-block sums of x
-// of the unit (Q4_K / Q5_K).
+// One task: for each of R units (row i at ub + i * rs; same unit column),
+// y[i] = sum over its 256 weights of w * x.  x: the column's 64 x chunks;
+// xs8 / fb8: the column's 8 sub-block sums of x and scale-back factors
+// (Q4_K / Q5_K).  Within a unit the order of every sum is fixed.
 // ---------------------------------------------------------------------------
-template <int F>
-__device__ __forceinline__ float unit_dot(const uint8_t *ub, const XRow &x, const float *xs8, const float *fb8);
+template <int F, int R>
+__device__ __forceinline__ void task_dot(const uint8_t *ub, int rs, const XRow &x, const float *xs8, const float *fb8,
+                                         float (&y)[R]);
 
 // Q4_0: 8 blocks; block b at byte 18b: f16 d, 16 bytes qs; element e < 16
 // is the low nibble of qs[e], e >= 16 the high nibble of qs[e - 16];
-// w = (nibble - 8) * d.
-template <>
-__device__ __forceinline__ float unit_dot<Q4_0>(const uint8_t *ub, const XRow &x, const float *, const float *) {
-    uint32_t r[36];
-    lds_words(r, ub);
+// w = (nibble - 8) * d.  Blocks are read in pairs through 40-byte windows
+// at 8-byte aligned word offsets 0, 8, 18, 26.
+template <int R>
+__device__ __forceinline__ void q40_task(const uint8_t *ub, int rs, const XRow &x, float (&y)[R]) {
     const float2 off = f2(-8388616.f, -8388616.f);   // -(2^23 + 8)
-    float y = 0.f;
 #pragma unroll
-    for (int b = 0; b < 8; ++b) {
-        const float d = f16_bits(half_at(r, 18 * b));
-        float2 acc = f2(0.f, 0.f);
+    for (int i = 0; i < R; ++i) y[i] = 0.f;
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            const uint32_t w = word_at(r, 18 * b + 2 + 4 * t);
-            acc = dot4(acc, w & 0x0F0F0F0Fu, off, x(8 * b + t));
-            acc = dot4(acc, (w >> 4) & 0x0F0F0F0Fu, off, x(8 * b + 4 + t));
+    for (int h = 0; h < 4; ++h) {
+        constexpr int kW0[4] = {0, 8, 18, 26};
+        const int w0 = kW0[h];
+        uint32_t r[R][10];
+#pragma unroll
+        for (int i = 0; i < R; ++i) lds_w64(r[i], ub + i * rs + 4 * w0);
+#pragma unroll
+        for (int bb = 0; bb < 2; ++bb) {
+            const int b = 2 * h + bb;
+            const int o = 18 * b - 4 * w0;
+            float2 acc[R];
+#pragma unroll
+            for (int i = 0; i < R; ++i) acc[i] = f2(0.f, 0.f);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const float4 xl = x(8 * b + t), xh = x(8 * b + 4 + t);
+#pragma unroll
+                for (int i = 0; i < R; ++i) {
+                    const uint32_t w = word_at(r[i], o + 2 + 4 * t);
+                    acc[i] = dot4(acc[i], w & 0x0F0F0F0Fu, off, xl);
+                    acc[i] = dot4(acc[i], (w >> 4) & 0x0F0F0F0Fu, off, xh);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < R; ++i) y[i] = fmaf(f16_bits(half_at(r[i], o)), acc[i].x + acc[i].y, y[i]);
         }
-        y = fmaf(d, acc.x + acc.y, y);
     }
-    return y;
 }
 
 // Q8_0: 8 blocks; block b at byte 34b: f16 d, 32 int8 q; w = q * d.  The
-// code byte with its sign bit flipped is q + 128.  Each half (4 blocks) is
-// read separately to bound the registers.
-template <>
-__device__ __forceinline__ float unit_dot<Q8_0>(const uint8_t *ub, const XRow &x, const float *, const float *) {
+// code byte with its sign bit flipped is q + 128.  Each block is read
+// through a 40-byte window at an 8-byte aligned word offset.
+template <int R>
+__device__ __forceinline__ void q80_task(const uint8_t *ub, int rs, const XRow &x, float (&y)[R]) {
     const float2 off = f2(-8388736.f, -8388736.f);   // -(2^23 + 128)
-    float y = 0.f;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        uint32_t r[36];
-        lds_words(r, ub + 128 * h);   // bytes 128h .. 128h + 143 cover blocks 4h .. 4h + 3
+    for (int i = 0; i < R; ++i) y[i] = 0.f;
 #pragma unroll
-        for (int bb = 0; bb < 4; ++bb) {
-            const int b = 4 * h + bb;
-            const int o = 34 * b - 128 * h;
-            const float d = f16_bits(half_at(r, o));
-            float2 acc = f2(0.f, 0.f);
+    for (int b = 0; b < 8; ++b) {
+        constexpr int kW0[8] = {0, 8, 16, 24, 34, 42, 50, 58};
+        const int w0 = kW0[b];
+        const int o = 34 * b - 4 * w0;
+        uint32_t r[R][10];
 #pragma unroll
-            for (int t = 0; t < 8; ++t)
-                acc = dot4(acc, word_at(r, o + 2 + 4 * t) ^ 0x80808080u, off, x(8 * b + t));
-            y = fmaf(d, acc.x + acc.y, y);
+        for (int i = 0; i < R; ++i) lds_w64(r[i], ub + i * rs + 4 * w0);
+        float2 acc[R];
+#pragma unroll
+        for (int i = 0; i < R; ++i) acc[i] = f2(0.f, 0.f);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            const float4 xv = x(8 * b + t);
+#pragma unroll
+            for (int i = 0; i < R; ++i) acc[i] = dot4(acc[i], word_at(r[i], o + 2 + 4 * t) ^ 0x80808080u, off, xv);
         }
+#pragma unroll
+        for (int i = 0; i < R; ++i) y[i] = fmaf(f16_bits(half_at(r[i], o)), acc[i].x + acc[i].y, y[i]);
     }
-    return y;
 }
 
 // Q4_K / Q5_K header: d, dmin, and the eight 6-bit (scale, min) pairs of the
-// 12 bytes at offset 4 (GGUF K-quant packing), as dsc[s] = d * sc_s and
-// dmn[s] = dmin * m_s (both exact in f32).
-__device__ __forceinline__ void kq_header(uint32_t r0, uint32_t w0, uint32_t w1, uint32_t w2, float (&dsc)[8],
-                                          float (&dmn)[8]) {
-    const float d = f16_bits(r0 & 0xFFFFu), dmin = f16_bits(r0 >> 16);
-    const uint32_t scA = w0 & 0x3F3F3F3Fu, mnA = w1 & 0x3F3F3F3Fu;
-    const uint32_t scB = (w2 & 0x0F0F0F0Fu) | ((w0 >> 2) & 0x30303030u);
-    const uint32_t mnB = ((w2 >> 4) & 0x0F0F0F0Fu) | ((w1 >> 2) & 0x30303030u);
-    const float2 m23 = f2(-8388608.f, -8388608.f);   // -(2^23)
-    float2 v;
-    v = __fadd2_rn(mag01(scA), m23); dsc[0] = d * v.x; dsc[1] = d * v.y;
-    v = __fadd2_rn(mag23(scA), m23); dsc[2] = d * v.x; dsc[3] = d * v.y;
-    v = __fadd2_rn(mag01(scB), m23); dsc[4] = d * v.x; dsc[5] = d * v.y;
-    v = __fadd2_rn(mag23(scB), m23); dsc[6] = d * v.x; dsc[7] = d * v.y;
-    v = __fadd2_rn(mag01(mnA), m23); dmn[0] = dmin * v.x; dmn[1] = dmin * v.y;
-    v = __fadd2_rn(mag23(mnA), m23); dmn[2] = dmin * v.x; dmn[3] = dmin * v.y;
-    v = __fadd2_rn(mag01(mnB), m23); dmn[4] = dmin * v.x; dmn[5] = dmin * v.y;
-    v = __fadd2_rn(mag23(mnB), m23); dmn[6] = dmin * v.x; dmn[7] = dmin * v.y;
-}
+// 12 bytes at offset 4 (GGUF K-quant packing).  Sub-blocks 0..3 take byte s
+// of (scA, mnA), sub-blocks 4..7 byte s - 4 of (scB, mnB).
+struct KHead {
+    float d, dmin;
+    uint32_t scA, mnA, scB, mnB;
+    __device__ __forceinline__ void load(const uint8_t *ub) {
+        const uint4 h = *reinterpret_cast<const uint4 *>(ub);
+        d = f16_bits(h.x & 0xFFFFu);
+        dmin = f16_bits(h.x >> 16);
+        scA = h.y & 0x3F3F3F3Fu;
+        mnA = h.z & 0x3F3F3F3Fu;
+        scB = (h.w & 0x0F0F0F0Fu) | ((h.y >> 2) & 0x30303030u);
+        mnB = ((h.w >> 4) & 0x0F0F0F0Fu) | ((h.z >> 2) & 0x30303030u);
+    }
+    // d * sc and dmin * m of sub-blocks 2p and 2p + 1 (exact in f32)
+    __device__ __forceinline__ void pair(int p, float2 &dsc, float2 &dmn) const {
+        const float2 m23 = f2(-8388608.f, -8388608.f);   // -(2^23)
+        const uint32_t sc = p < 2 ? scA : scB, mn = p < 2 ? mnA : mnB;
+        const float2 vs = __fadd2_rn((p & 1) ? mag23(sc) : mag01(sc), m23);
+        const float2 vm = __fadd2_rn((p & 1) ? mag23(mn) : mag01(mn), m23);
+        dsc = f2(d * vs.x, d * vs.y);
+        dmn = f2(dmin * vm.x, dmin * vm.y);
+    }
+};
 
 // Q4_K: d @0, dmin @2, scales @4..15, qs @16..143; element e = 32 s + l is
 // the low (s even) or high (s odd) nibble of qs[32 (s / 2) + l];
 // w = d sc_s q - dmin m_s, summed as dsc_s * sum(q x) - dmn_s * sum(x).
-// sum(q x) from subnormal codes and the block-scaled x (fb8: the unit's 8
+// sum(q x) from subnormal codes and the block-scaled x (fb8: the column's 8
 // scale-back factors), sum(x) from the f32 sums of the unscaled x (xs8).
-template <>
-__device__ __forceinline__ float unit_dot<Q4_K>(const uint8_t *ub, const XRow &x, const float *xs8,
-                                                const float *fb8) {
-    uint32_t r[36];
-    lds_words(r, ub);
-    float dsc[8], dmn[8];
-    kq_header(r[0], r[1], r[2], r[3], dsc, dmn);
-    const float4 xa = *reinterpret_cast<const float4 *>(xs8), xb = *reinterpret_cast<const float4 *>(xs8 + 4);
-    const float xsum[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
-    const float4 fa = *reinterpret_cast<const float4 *>(fb8), fc = *reinterpret_cast<const float4 *>(fb8 + 4);
-    const float fb[8] = {fa.x, fa.y, fa.z, fa.w, fc.x, fc.y, fc.z, fc.w};
-    float y = 0.f;
+template <int R>
+__device__ __forceinline__ void q4k_task(const uint8_t *ub, int rs, const XRow &x, const float *xs8, const float *fb8,
+                                         float (&y)[R]) {
+    KHead hd[R];
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+        hd[i].load(ub + i * rs);
+        y[i] = 0.f;
+    }
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
-        float2 alo = f2(0.f, 0.f), ahi = f2(0.f, 0.f);
+        uint32_t r[R][8];
+#pragma unroll
+        for (int i = 0; i < R; ++i) lds_w128(r[i], ub + i * rs + 16 + 32 * p);
+        float2 alo[R], ahi[R];
+#pragma unroll
+        for (int i = 0; i < R; ++i) alo[i] = ahi[i] = f2(0.f, 0.f);
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
-            const uint32_t w = r[4 + 8 * p + t];
-            alo = dot4s(alo, w & 0x0F0F0F0Fu, x(16 * p + t));
-            ahi = dot4s(ahi, (w >> 4) & 0x0F0F0F0Fu, x(16 * p + 8 + t));
+            const float4 xl = x(16 * p + t), xh = x(16 * p + 8 + t);
+#pragma unroll
+            for (int i = 0; i < R; ++i) {
+                alo[i] = dot4s(alo[i], r[i][t] & 0x0F0F0F0Fu, xl);
+                ahi[i] = dot4s(ahi[i], (r[i][t] >> 4) & 0x0F0F0F0Fu, xh);
+            }
         }
-        y = fmaf(dsc[2 * p], unscale(alo.x + alo.y, fb[2 * p]), y);
-        y = fmaf(-dmn[2 * p], xsum[2 * p], y);
-        y = fmaf(dsc[2 * p + 1], unscale(ahi.x + ahi.y, fb[2 * p + 1]), y);
-        y = fmaf(-dmn[2 * p + 1], xsum[2 * p + 1], y);
+        const float sl = xs8[2 * p], sh = xs8[2 * p + 1], fl = fb8[2 * p], fh = fb8[2 * p + 1];
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            float2 dsc, dmn;
+            hd[i].pair(p, dsc, dmn);
+            y[i] = fmaf(dsc.x, unscale(alo[i].x + alo[i].y, fl), y[i]);
+            y[i] = fmaf(-dmn.x, sl, y[i]);
+            y[i] = fmaf(dsc.y, unscale(ahi[i].x + ahi[i].y, fh), y[i]);
+            y[i] = fmaf(-dmn.y, sh, y[i]);
+        }
     }
-    return y;
 }
 
 // Q5_K: as Q4_K with qh[32] @16 and qs @48; bit s of qh[l] is bit 4 of
 // element 32 s + l.
-template <>
-__device__ __forceinline__ float unit_dot<Q5_K>(const uint8_t *ub, const XRow &x, const float *xs8,
-                                                const float *fb8) {
-    uint32_t r[44];
-    lds_words(r, ub);
-    float dsc[8], dmn[8];
-    kq_header(r[0], r[1], r[2], r[3], dsc, dmn);
-    const float4 xa = *reinterpret_cast<const float4 *>(xs8), xb = *reinterpret_cast<const float4 *>(xs8 + 4);
-    const float xsum[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
-    const float4 fa = *reinterpret_cast<const float4 *>(fb8), fc = *reinterpret_cast<const float4 *>(fb8 + 4);
-    const float fb[8] = {fa.x, fa.y, fa.z, fa.w, fc.x, fc.y, fc.z, fc.w};
-    float y = 0.f;
+template <int R>
+__device__ __forceinline__ void q5k_task(const uint8_t *ub, int rs, const XRow &x, const float *xs8, const float *fb8,
+                                         float (&y)[R]) {
+    KHead hd[R];
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+        hd[i].load(ub + i * rs);
+        y[i] = 0.f;
+    }
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
-        float2 alo = f2(0.f, 0.f), ahi = f2(0.f, 0.f);
+        float2 alo[R], ahi[R];
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-            const uint32_t w = r[12 + 8 * p + t], qh = r[4 + t];
-            const uint32_t qlo = (w & 0x0F0F0F0Fu) | (((qh >> (2 * p)) & 0x01010101u) << 4);
-            const uint32_t qhi = ((w >> 4) & 0x0F0F0F0Fu) | (((qh >> (2 * p + 1)) & 0x01010101u) << 4);
-            alo = dot4s(alo, qlo, x(16 * p + t));
-            ahi = dot4s(ahi, qhi, x(16 * p + 8 + t));
+        for (int i = 0; i < R; ++i) alo[i] = ahi[i] = f2(0.f, 0.f);
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {   // words 4 hf .. 4 hf + 3 of the 32-byte pieces
+            uint32_t q[R][4], qh[R][4];
+#pragma unroll
+            for (int i = 0; i < R; ++i) {
+                lds_w128(q[i], ub + i * rs + 48 + 32 * p + 16 * hf);
+                lds_w128(qh[i], ub + i * rs + 16 + 16 * hf);
+            }
+#pragma unroll
+            for (int tt = 0; tt < 4; ++tt) {
+                const int t = 4 * hf + tt;
+                const float4 xl = x(16 * p + t), xh = x(16 * p + 8 + t);
+#pragma unroll
+                for (int i = 0; i < R; ++i) {
+                    const uint32_t w = q[i][tt], hb = qh[i][tt];
+                    const uint32_t qlo = (w & 0x0F0F0F0Fu) | (((hb >> (2 * p)) & 0x01010101u) << 4);
+                    const uint32_t qhi = ((w >> 4) & 0x0F0F0F0Fu) | (((hb >> (2 * p + 1)) & 0x01010101u) << 4);
+                    alo[i] = dot4s(alo[i], qlo, xl);
+                    ahi[i] = dot4s(ahi[i], qhi, xh);
+                }
+            }
         }
-        y = fmaf(dsc[2 * p], unscale(alo.x + alo.y, fb[2 * p]), y);
-        y = fmaf(-dmn[2 * p], xsum[2 * p], y);
-        y = fmaf(dsc[2 * p + 1], unscale(ahi.x + ahi.y, fb[2 * p + 1]), y);
-        y = fmaf(-dmn[2 * p + 1], xsum[2 * p + 1], y);
+        const float sl = xs8[2 * p], sh = xs8[2 * p + 1], fl = fb8[2 * p], fh = fb8[2 * p + 1];
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            float2 dsc, dmn;
+            hd[i].pair(p, dsc, dmn);
+            y[i] = fmaf(dsc.x, unscale(alo[i].x + alo[i].y, fl), y[i]);
+            y[i] = fmaf(-dmn.x, sl, y[i]);
+            y[i] = fmaf(dsc.y, unscale(ahi[i].x + ahi[i].y, fh), y[i]);
+            y[i] = fmaf(-dmn.y, sh, y[i]);
+        }
     }
-    return y;
 }
 
 // Q6_K: ql[128] @0, qh[64] @128, int8 scales[16] @192, f16 d @208.
 // Element e = 128 h + 32 j + l: low 4 bits from ql[64 h + 32 (j % 2) + l]
 // (low nibble for j < 2, high for j >= 2), bits 4..5 = bits 2j, 2j+1 of
-// qh[32 h + l]; w = d * scales[e / 16] * (q - 32).  The unit starts at an
+// qh[32 h + l]; w = d * scales[e / 16] * (q - 32).  A unit starts at an
 // even byte; words are assembled from 4-byte aligned loads.
-template <>
-__device__ __forceinline__ float unit_dot<Q6_K>(const uint8_t *ub, const XRow &x, const float *, const float *) {
-    const uint32_t sh = (uint32_t)(reinterpret_cast<uintptr_t>(ub) & 2u) * 8u;   // 0 or 16 bits
-    const uint32_t *wp = reinterpret_cast<const uint32_t *>(ub - (sh >> 3));
-    auto W = [&](int i) { return __funnelshift_r(wp[i], wp[i + 1], sh); };
-    const float d = f16_bits(W(52));
-    float ds[16];
-    const float2 m128 = f2(-8388736.f, -8388736.f);   // -(2^23 + 128)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint32_t s = W(48 + i) ^ 0x80808080u;
-        const float2 a = __fadd2_rn(mag01(s), m128), b = __fadd2_rn(mag23(s), m128);
-        ds[4 * i] = d * a.x;
-        ds[4 * i + 1] = d * a.y;
-        ds[4 * i + 2] = d * b.x;
-        ds[4 * i + 3] = d * b.y;
+struct Q6Row {
+    const uint32_t *wp;
+    uint32_t sh;
+    __device__ __forceinline__ explicit Q6Row(const uint8_t *ub) {
+        sh = (uint32_t)(reinterpret_cast<uintptr_t>(ub) & 2u) * 8u;   // 0 or 16 bits
+        wp = reinterpret_cast<const uint32_t *>(ub - (sh >> 3));
     }
+    __device__ __forceinline__ uint32_t operator()(int i) const { return __funnelshift_r(wp[i], wp[i + 1], sh); }
+};
+
+template <int R>
+__device__ __forceinline__ void q6k_task(const uint8_t *ub, int rs, const XRow &x, float (&y)[R]) {
     const float2 off = f2(-8388640.f, -8388640.f);   // -(2^23 + 32)
-    float y = 0.f;
+    const float2 m128 = f2(-8388736.f, -8388736.f);  // -(2^23 + 128)
+    float d[R];
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+        d[i] = f16_bits(Q6Row(ub + i * rs)(52));
+        y[i] = 0.f;
+    }
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-        float2 acc[4][2];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc[j][0] = acc[j][1] = f2(0.f, 0.f);
+        for (int hv = 0; hv < 2; ++hv) {
+            float2 acc[R][4];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const uint32_t qa = W(16 * h + u), qb = W(16 * h + 8 + u), qh = W(32 + 8 * h + u);
-            const uint32_t q0 = (qa & 0x0F0F0F0Fu) | ((qh << 4) & 0x30303030u);
-            const uint32_t q1 = (qb & 0x0F0F0F0Fu) | ((qh << 2) & 0x30303030u);
-            const uint32_t q2 = ((qa >> 4) & 0x0F0F0F0Fu) | (qh & 0x30303030u);
-            const uint32_t q3 = ((qb >> 4) & 0x0F0F0F0Fu) | ((qh >> 2) & 0x30303030u);
-            const int hv = u >> 2;
-            acc[0][hv] = dot4(acc[0][hv], q0, off, x(32 * h + u));
-            acc[1][hv] = dot4(acc[1][hv], q1, off, x(32 * h + 8 + u));
-            acc[2][hv] = dot4(acc[2][hv], q2, off, x(32 * h + 16 + u));
-            acc[3][hv] = dot4(acc[3][hv], q3, off, x(32 * h + 24 + u));
-        }
+            for (int i = 0; i < R; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            y = fmaf(ds[8 * h + 2 * j], acc[j][0].x + acc[j][0].y, y);
-            y = fmaf(ds[8 * h + 2 * j + 1], acc[j][1].x + acc[j][1].y, y);
+                for (int j = 0; j < 4; ++j) acc[i][j] = f2(0.f, 0.f);
+#pragma unroll
+            for (int uu = 0; uu < 4; ++uu) {
+                const int u = 4 * hv + uu;
+                const float4 x0 = x(32 * h + u), x1 = x(32 * h + 8 + u), x2 = x(32 * h + 16 + u),
+                             x3 = x(32 * h + 24 + u);
+#pragma unroll
+                for (int i = 0; i < R; ++i) {
+                    const Q6Row W(ub + i * rs);
+                    const uint32_t qa = W(16 * h + u), qb = W(16 * h + 8 + u), qh = W(32 + 8 * h + u);
+                    const uint32_t q0 = (qa & 0x0F0F0F0Fu) | ((qh << 4) & 0x30303030u);
+                    const uint32_t q1 = (qb & 0x0F0F0F0Fu) | ((qh << 2) & 0x30303030u);
+                    const uint32_t q2 = ((qa >> 4) & 0x0F0F0F0Fu) | (qh & 0x30303030u);
+                    const uint32_t q3 = ((qb >> 4) & 0x0F0F0F0Fu) | ((qh >> 2) & 0x30303030u);
+                    acc[i][0] = dot4(acc[i][0], q0, off, x0);
+                    acc[i][1] = dot4(acc[i][1], q1, off, x1);
+                    acc[i][2] = dot4(acc[i][2], q2, off, x2);
+                    acc[i][3] = dot4(acc[i][3], q3, off, x3);
+                }
+            }
+            // scales 8h + 2j + hv, j = 0..3: bytes hv, 2 + hv of words 48 + 2h, 49 + 2h
+#pragma unroll
+            for (int i = 0; i < R; ++i) {
+                const Q6Row W(ub + i * rs);
+                const uint32_t sa = W(48 + 2 * h) ^ 0x80808080u, sb = W(49 + 2 * h) ^ 0x80808080u;
+                const float2 s01 = __fadd2_rn(f2(mag(sa, hv), mag(sa, 2 + hv)), m128);
+                const float2 s23 = __fadd2_rn(f2(mag(sb, hv), mag(sb, 2 + hv)), m128);
+                y[i] = fmaf(d[i] * s01.x, acc[i][0].x + acc[i][0].y, y[i]);
+                y[i] = fmaf(d[i] * s01.y, acc[i][1].x + acc[i][1].y, y[i]);
+                y[i] = fmaf(d[i] * s23.x, acc[i][2].x + acc[i][2].y, y[i]);
+                y[i] = fmaf(d[i] * s23.y, acc[i][3].x + acc[i][3].y, y[i]);
+            }
         }
     }
-    return y;
+}
+
+template <int F, int R>
+__device__ __forceinline__ void task_dot(const uint8_t *ub, int rs, const XRow &x, const float *xs8, const float *fb8,
+                                         float (&y)[R]) {
+    if constexpr (F == Q4_0) q40_task<R>(ub, rs, x, y);
+    else if constexpr (F == Q8_0) q80_task<R>(ub, rs, x, y);
+    else if constexpr (F == Q4_K) q4k_task<R>(ub, rs, x, xs8, fb8, y);
+    else if constexpr (F == Q5_K) q5k_task<R>(ub, rs, x, xs8, fb8, y);
+    else q6k_task<R>(ub, rs, x, y);
 }
 
 // ---------------------------------------------------------------------------
@@ -359,21 +461,26 @@ __device__ __forceinline__ bool warp_wait(volatile unsigned *abort_flag, uint64_
     return __all_sync(0xffffffffu, ok);
 }
 
-template <int F, bool XBF16>
+// A stage is one contiguous byte range of W when its rows are consecutive
+// (R = 1) or it holds whole row groups (U divides 32).
+__host__ __device__ constexpr bool stage_contiguous(int R, int U) { return R == 1 || kLanes % U == 0; }
+
+template <int F, bool XBF16, int R>
 __global__ void __launch_bounds__(512, 1) gemv_stream_kernel(const __grid_constant__ StreamArgs a) {
     extern __shared__ __align__(1024) uint8_t sm[];
     constexpr int UB = UnitBytes<F>::B;
-    constexpr int SLOT = slot_bytes(UB);
+    constexpr int SLOT = slot_bytes(UB, R);
     const int nw = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int S = a.S;
     const int U = a.K >> 8;                                     // units per row
     const int64_t r0 = (int64_t)blockIdx.x * a.M / gridDim.x;
     const int64_t r1 = (int64_t)(blockIdx.x + 1) * a.M / gridDim.x;
     const int nrows = (int)(r1 - r0);
-    const int nunits = nrows * U;
-    const int nst = (nunits + kLanes - 1) / kLanes;            // stages of the CTA
+    const int ngrp = (nrows + R - 1) / R;                       // row groups (the last may be short)
+    const int ntasks = ngrp * U;
+    const int nst = (ntasks + kLanes - 1) / kLanes;            // stages of the CTA
     const uint8_t *wcta = a.W + r0 * (int64_t)U * UB;
-    const int64_t cta_bytes = (int64_t)nunits * UB;
+    const bool contiguous = stage_contiguous(R, U);
 
     float *xs = reinterpret_cast<float *>(sm + a.off_x);
     float *xsum = reinterpret_cast<float *>(sm + a.off_xsum);
@@ -391,18 +498,55 @@ __global__ void __launch_bounds__(512, 1) gemv_stream_kernel(const __grid_consta
 
     // this warp's stages: s = warp + nw * j, j = 0 .. my_nst - 1
     const int my_nst = warp < nst ? (nst - 1 - warp) / nw + 1 : 0;
+    // Stage layout in its slot: the stage's tasks split into segments by
+    // row group; segment [L, E) of group g holds its R rows one after the
+    // other, n = E - L units each: unit (lane l, row i) at R L + i n + (l - L).
+    // Warp-collective.
     auto issue = [&](int j) {
         const int s = warp + nw * j;
-        const int64_t off = (int64_t)s * kLanes * UB;
-        const int64_t rem = cta_bytes - off;
-        const uint32_t bytes = (uint32_t)(rem < kLanes * UB ? rem : kLanes * UB);
+        const int t0 = s * kLanes;
+        const int te = min(t0 + kLanes, ntasks);
         const int slot = warp * S + j % S;
-        mbar_arrive_expect_tx(&bars[slot], bytes);
-        tma_load_1d(sm + (size_t)slot * SLOT, wcta + off, bytes, &bars[slot]);
+        uint8_t *dst = sm + (size_t)slot * SLOT;
+        uint64_t *bar = &bars[slot];
+        if (contiguous) {
+            if (lane == 0) {
+                int64_t u0, nu;   // first unit (in W's order) and unit count
+                if (R == 1) {
+                    u0 = t0;
+                    nu = te - t0;
+                } else {
+                    const int ra = (t0 / U) * R, rb = min((te / U) * R, nrows);
+                    u0 = (int64_t)ra * U;
+                    nu = (int64_t)(rb - ra) * U;
+                }
+                const uint32_t bytes = (uint32_t)(nu * UB);
+                mbar_arrive_expect_tx(bar, bytes);
+                tma_load_1d(dst, wcta + u0 * UB, bytes, bar);
+            }
+        } else {
+            const int g0 = t0 / U;
+            if (lane == 0) {
+                uint32_t bytes = 0;
+                for (int g = g0; g * U < te; ++g) {
+                    const int n = min(te, (g + 1) * U) - max(t0, g * U);
+                    bytes += (uint32_t)(n * min(R, nrows - g * R) * UB);
+                }
+                mbar_arrive_expect_tx(bar, bytes);
+            }
+            __syncwarp();
+            for (int k = lane;; k += kLanes) {   // piece k: row k % R of segment k / R
+                const int g = g0 + k / R, i = k % R;
+                if (g * U >= te) break;
+                if (g * R + i >= nrows) continue;
+                const int L = max(t0, g * U) - t0, n = min(te, (g + 1) * U) - t0 - L;
+                const uint8_t *src = wcta + ((int64_t)(g * R + i) * U + (t0 + L - g * U)) * UB;
+                tma_load_1d(dst + (size_t)(R * L + i * n) * UB, src, (uint32_t)(n * UB), bar);
+            }
+        }
     };
     // weights first: they do not depend on the preceding grid
-    if (lane == 0)
-        for (int j = 0; j < S && j < my_nst; ++j) issue(j);
+    for (int j = 0; j < S && j < my_nst; ++j) issue(j);
 
     pdl_wait();   // X and Y are ordered behind the preceding grid
 
@@ -474,37 +618,55 @@ __global__ void __launch_bounds__(512, 1) gemv_stream_kernel(const __grid_consta
         const int slot = warp * S + j % S;
         if (!warp_wait(abort_flag, &bars[slot], (uint32_t)(j / S) & 1u, a.limit)) break;
         const int s = warp + nw * j;
-        const int u = s * kLanes + lane;
-        float v = 0.f;
-        int key = 0x7FFFFFFF;
-        if (u < nunits) {
-            key = u / U;                   // row of the unit (within the CTA)
-            const int p = u - key * U;     // unit within the row
+        const int t0 = s * kLanes;
+        const int te = min(t0 + kLanes, ntasks);
+        const int t = t0 + lane;
+        float v[R];
+        int key = 0x7FFFFFFF, g = 0;
+        if (t < te) {
+            g = t / U;                               // row group of the task
+            const int p = t - g * U;                 // unit column
+            const int L = max(t0, g * U) - t0, n = min(te, (g + 1) * U) - t0 - L;
+            key = g;
             const XRow xr(xs4 + (p << 6), p & 7);
-            v = unit_dot<F>(sm + (size_t)slot * SLOT + lane * UB, xr, xsum + 8 * p, xsum + (a.K >> 5) + 8 * p);
+            task_dot<F, R>(sm + (size_t)slot * SLOT + (size_t)(R * L + (lane - L)) * UB, n * UB, xr, xsum + 8 * p,
+                           xsum + (a.K >> 5) + 8 * p, v);
+        } else {
+#pragma unroll
+            for (int i = 0; i < R; ++i) v[i] = 0.f;
         }
         __syncwarp();
-        if (lane == 0 && j + S < my_nst) issue(j + S);   // every lane has read the slot
+        if (j + S < my_nst) issue(j + S);   // every lane has read the slot
         done = j + 1;
-        // segmented reduction by row: each row's first lane of the stage
-        // ends up with the stage's sum for that row
+        // segmented reduction by row group: each group's first lane of the
+        // stage ends up with the stage's sums for the group's rows
 #pragma unroll
         for (int o = 1; o < kLanes; o <<= 1) {
-            const float vo = __shfl_down_sync(0xffffffffu, v, o);
             const int ko = __shfl_down_sync(0xffffffffu, key, o);
-            if (lane + o < kLanes && ko == key) v += vo;
+            const bool same = lane + o < kLanes && ko == key;
+#pragma unroll
+            for (int i = 0; i < R; ++i) {
+                const float vo = __shfl_down_sync(0xffffffffu, v[i], o);
+                if (same) v[i] += vo;
+            }
         }
         const int kp = __shfl_up_sync(0xffffffffu, key, 1);
-        if (u < nunits && (lane == 0 || kp != key)) {
-            const bool starts = key * U >= s * kLanes;
-            const bool ends = key * U + U <= (s + 1) * kLanes;
-            if (starts && ends) {
-                if (amax)
-                    amax_fold(best, v, (int)(r0 + key));
-                else
-                    Yc[key] = v;
-            } else
-                part[2 * s + (starts ? 1 : 0)] = v;   // 0: row begun earlier, 1: row continues later
+        if (t < te && (lane == 0 || kp != key)) {
+            const bool starts = g * U >= t0;
+            const bool ends = (g + 1) * U <= t0 + kLanes;
+#pragma unroll
+            for (int i = 0; i < R; ++i) {
+                const int row = g * R + i;
+                if (row >= nrows) break;
+                if (starts && ends) {
+                    if (amax)
+                        amax_fold(best, v[i], (int)(r0 + row));
+                    else
+                        Yc[row] = v[i];
+                } else {
+                    part[(2 * s + (starts ? 1 : 0)) * R + i] = v[i];   // 0: begun earlier, 1: continues later
+                }
+            }
         }
     }
     // copies still in flight (only after an abort): wait for them before exit
@@ -519,12 +681,13 @@ __global__ void __launch_bounds__(512, 1) gemv_stream_kernel(const __grid_consta
         if (threadIdx.x == 0) report_status(a.status, kStatusTimeout);
         return;
     }
-    // rows that cross stages: stage partials in stage order
+    // row groups that cross stages: stage partials in stage order
     for (int rl = threadIdx.x; rl < nrows; rl += blockDim.x) {
-        const int sa = (rl * U) / kLanes, sb = (rl * U + U - 1) / kLanes;
+        const int g = rl / R, i = rl - g * R;
+        const int sa = (g * U) / kLanes, sb = (g * U + U - 1) / kLanes;
         if (sa == sb) continue;
-        float v = part[2 * sa + 1];
-        for (int s = sa + 1; s <= sb; ++s) v += part[2 * s];
+        float v = part[(2 * sa + 1) * R + i];
+        for (int s = sa + 1; s <= sb; ++s) v += part[2 * s * R + i];
         if (amax)
             amax_fold(best, v, (int)(r0 + rl));
         else
@@ -558,13 +721,14 @@ int unit_bytes_of(int fmt) {
 constexpr int kSmemMax = 232448 - 1024;   // the opt-in maximum, less room for static shared words
 constexpr int kSmemPerSM = 233472;        // shared memory of one SM (two CTAs: each also has 1 KB reserved)
 
-// Shared-memory layout for nw warps, S slots, K and up to nst stages.
+// Shared-memory layout for R rows per task, nw warps, S slots, K and up to
+// nst stages.
 struct StreamLayout {
     int off_x, off_xsum, off_part, off_bar, off_flag, total;
 };
-StreamLayout stream_layout(int fmt, int nw, int S, int64_t K, int64_t nst) {
+StreamLayout stream_layout(int fmt, int R, int nw, int S, int64_t K, int64_t nst) {
     StreamLayout L;
-    const int slot = slot_bytes(unit_bytes_of(fmt));
+    const int slot = slot_bytes(unit_bytes_of(fmt), R);
     int64_t o = (int64_t)nw * S * slot;
     L.off_x = (int)o;
     o += K * 4;
@@ -572,7 +736,7 @@ StreamLayout stream_layout(int fmt, int nw, int S, int64_t K, int64_t nst) {
     o += kmin_fmt(fmt) ? K / 4 : 0;   // per 32-element block: the sum of x, then the scale-back factor
     o = (o + 15) / 16 * 16;
     L.off_part = (int)o;
-    o += (nst * 8 + 15) / 16 * 16;
+    o += (nst * 8 * R + 15) / 16 * 16;
     L.off_bar = (int)o;
     o += (int64_t)nw * S * 8;
     L.off_flag = (int)o;
@@ -581,9 +745,9 @@ StreamLayout stream_layout(int fmt, int nw, int S, int64_t K, int64_t nst) {
     return L;
 }
 
-template <int F, bool XBF16>
+template <int F, bool XBF16, int R>
 cudaError_t launch_typed(const StreamPlan &p, const StreamArgs &a, bool pdl, cudaStream_t st) {
-    auto kern = gemv_stream_kernel<F, XBF16>;
+    auto kern = gemv_stream_kernel<F, XBF16, R>;
     static std::atomic<int> configured[64];   // largest dynamic shared memory set, per device
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -608,43 +772,76 @@ cudaError_t launch_typed(const StreamPlan &p, const StreamArgs &a, bool pdl, cud
     return launched(cudaGetLastError());
 }
 
+template <int F, bool XBF16>
+cudaError_t launch_rows(const StreamPlan &p, const StreamArgs &a, bool pdl, cudaStream_t st) {
+    switch (p.R) {
+    case 1: return launch_typed<F, XBF16, 1>(p, a, pdl, st);
+    case 2: return launch_typed<F, XBF16, 2>(p, a, pdl, st);
+    case 4: return launch_typed<F, XBF16, 4>(p, a, pdl, st);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
 template <int F>
 cudaError_t launch_fmt(const StreamPlan &p, const StreamArgs &a, int xbf16, bool pdl, cudaStream_t st) {
-    return xbf16 ? launch_typed<F, true>(p, a, pdl, st) : launch_typed<F, false>(p, a, pdl, st);
+    return xbf16 ? launch_rows<F, true>(p, a, pdl, st) : launch_rows<F, false>(p, a, pdl, st);
 }
 
 }  // namespace
 
-bool plan_gemv_stream(int fmt, int64_t M, int64_t K, int num_sms, int force_warps, StreamPlan &p) {
+bool plan_gemv_stream(int fmt, int64_t M, int64_t K, int num_sms, const StreamForce &force, StreamPlan &p) {
     const int ub = unit_bytes_of(fmt);
     if (!ub || K % 256 || M < 1 || num_sms < 1 || K > (1 << 15)) return false;
     if ((K / 256 * ub) % 16) return false;   // rows must start 16-byte aligned
-    // Short launches (K <= 4096, at most 64 MB of weights) run two CTAs of
-    // at most 8 warps per SM: when one launch follows another on the stream,
-    // the next launch's CTAs then start (and stream their weights) on SMs
-    // where the previous launch's CTAs are still finishing.  Measured on
-    // Q4_0 / Q8_0 / Q4_K rows of 4096: 5-6% shorter launches; long rows
-    // (every CTA stages all of X) and long launches do better with one.
-    const int64_t wbytes = M * (K / 256) * ub;
-    int cps = K <= 4096 && wbytes <= (64ll << 20) ? 2 : 1;
-    if (force_warps > 16 / cps) cps = 1;
+    const int U = (int)(K / 256);
+    const int64_t wbytes = M * U * ub;
+    const bool short_launch = wbytes <= (64ll << 20);
+    // Rows per task (measured on the Llama-3-8B decode shapes, GB300): two
+    // where every SM still gets at least 4 stages of 32 tasks and a stage is
+    // one contiguous copy; of the piecewise stages only the offset-free
+    // K-quants (Q4_K, Q5_K: the fewest ALU instructions per weight, so the
+    // X reads weigh most) gain from two.  Four rows per task need slots so
+    // large that too few warps fit: only on request.  Piecewise stages need
+    // 16-byte aligned units (all formats but Q6_K).
+    int R = 1;
+    if ((double)M * U / (2.0 * kLanes * num_sms) >= 4.0 &&
+        (stage_contiguous(2, U) || (kmin_fmt(fmt) && ub % 16 == 0)))
+        R = 2;
+    if (force.r) {
+        if (force.r != 1 && force.r != 2 && force.r != 4) return false;
+        if (!stage_contiguous(force.r, U) && ub % 16) return false;
+        R = force.r;
+    }
+    // Two CTAs per SM for launches of short rows (K <= 4096: X is cheap to
+    // stage twice) up to 64 MB; one otherwise.
+    int cps = K <= 4096 && short_launch ? 2 : 1;
+    if (force.cps == 1 || force.cps == 2) cps = force.cps;
+    if (force.warps > 16 / cps || force.slots > 3) return false;
     const int lim = cps == 2 ? kSmemPerSM / 2 - 3072 : kSmemMax;
+    // Every CTA takes more than 1 / (cps + 1) of the SM's shared memory, so
+    // that no SM ever holds more than cps CTAs of one launch.  Without that
+    // floor, when launches follow one another (programmatic dependent
+    // launch), the CTAs of the next launch pile up on the SMs that free up
+    // first and leave others idle; measured on a 32-layer decoder sequence.
+    const int floor_smem = kSmemPerSM / (cps + 1) + 1024;
     int64_t grid = M < (int64_t)cps * num_sms ? M : (int64_t)cps * num_sms;
     for (int attempt = 0; attempt < 8; ++attempt) {
         const int64_t rows = (M + grid - 1) / grid;
-        const int64_t nst = (rows * (K / 256) + kLanes - 1) / kLanes;
-        for (int nw : {16, 12, 8, 4}) {
-            if (force_warps ? nw != force_warps : nw > 16 / cps) continue;
-            for (int S : {3, 2}) {
-                const StreamLayout L = stream_layout(fmt, nw, S, K, nst);
-                if (L.total <= lim) {
-                    p.grid = (int)grid;
-                    p.warps = nw;
-                    p.S = S;
-                    p.smem = L.total;
-                    return true;
-                }
+        const int64_t nst = ((rows + R - 1) / R * U + kLanes - 1) / kLanes;
+        // the most warps (at most 16 per SM) with one slot each: measured
+        // faster than fewer warps with 2 or 3 slots
+        const int S = force.slots ? force.slots : 1;
+        for (int nw = force.warps ? force.warps : 16 / cps; nw >= 1; --nw) {
+            const StreamLayout L = stream_layout(fmt, R, nw, S, K, nst);
+            if (L.total <= lim) {
+                p.grid = (int)grid;
+                p.warps = nw;
+                p.S = S;
+                p.R = R;
+                p.smem = std::max(L.total, std::min(floor_smem, lim));
+                return true;
             }
+            if (force.warps) break;
         }
         if (grid >= M) break;
         grid = grid * 2 < M ? grid * 2 : M;   // more, smaller CTAs: fewer partials each
@@ -656,8 +853,8 @@ cudaError_t launch_gemv_stream(int fmt, const StreamPlan &p, const uint8_t *W, i
                                int xbf16, float *Y, bool pdl, unsigned *status, uint64_t limit, cudaStream_t st,
                                unsigned long long *amax_ws, int32_t *idx, float *val) {
     const int64_t rows = (M + p.grid - 1) / p.grid;
-    const int64_t nst = (rows * (K / 256) + kLanes - 1) / kLanes;
-    const StreamLayout L = stream_layout(fmt, p.warps, p.S, K, nst);
+    const int64_t nst = ((rows + p.R - 1) / p.R * (K / 256) + kLanes - 1) / kLanes;
+    const StreamLayout L = stream_layout(fmt, p.R, p.warps, p.S, K, nst);
     if (L.total > p.smem) return cudaErrorInvalidValue;
     StreamArgs a;
     a.W = W;

@@ -63,17 +63,23 @@ cudaError_t launch_gemv_mma(int fmt, const GemvPlan &plan, const GemvSegs &segs,
                             float *val = nullptr);
 
 // Streaming decode GEMV for N = 1 (K % 256 == 0, K <= 32768, 16-byte
-// aligned W, rows and X): one CTA of `warps` warps per SM owns whole rows,
-// each warp streams 32-unit stages of them through S shared-memory slots.
+// aligned W, rows and X): CTAs of `warps` warps own whole rows; each warp
+// streams stages of 32 tasks (R rows x one 256-weight column each) through
+// S shared-memory slots.
 struct StreamPlan {
     int grid;
     int warps;
     int S;
+    int R;      // rows per task: 1, 2 or 4
     int smem;   // dynamic shared memory bytes
 };
-// false: the shape does not fit the kernel (another GEMV kernel runs).
-// force_warps > 0 requests that many warps per CTA.
-bool plan_gemv_stream(int fmt, int64_t M, int64_t K, int num_sms, int force_warps, StreamPlan &p);
+// Requested plan parameters; 0 = chosen by the planner.  cps: CTAs per SM.
+struct StreamForce {
+    int r, warps, slots, cps;
+};
+// false: the shape does not fit the kernel (another GEMV kernel runs), or
+// a forced parameter cannot be met.
+bool plan_gemv_stream(int fmt, int64_t M, int64_t K, int num_sms, const StreamForce &force, StreamPlan &p);
 // y[M] = W x.  pdl: programmatic dependent of the preceding kernel (the
 // weight copies start before it ends; X and Y wait for it).
 // amax_ws != nullptr: argmax mode as in launch_gemv_mma (Y is not written).

@@ -31,7 +31,7 @@ EXPORTS = ("qmm_gemv", "qmm_gemv_argmax", "qmm_gemv_multi", "qmm_gemm", "qmm_gem
            "qmm_set_wait_limit", "qmm_set_static_weights", "qmm_set_gemv_i8", "qmm_set_gemv_tc", "qmm_quantize_q8_0",
            "qmm_gemv_preq", "qmm_q8act_workspace_bytes", "qmm_gemv_q8act", "qmm_gemv_swiglu",
            "qmm_gemm_q8act_workspace_bytes", "qmm_gemm_q8act", "qmm_gemm_swiglu_workspace_bytes", "qmm_gemm_swiglu",
-           "qmm_kernel_launches")
+           "qmm_kernel_launches", "qmm_set_gemv_stream", "qmm_gemv_stream_plan")
 
 _lock = threading.Lock()
 _lib = None
@@ -78,6 +78,9 @@ def load() -> ctypes.CDLL:
         lib.qmm_set_gemv_i8.restype = None
         lib.qmm_set_gemv_tc.argtypes = [ctypes.c_int]
         lib.qmm_set_gemv_tc.restype = None
+        lib.qmm_set_gemv_stream.argtypes = [ci, ci, ci, ci]
+        lib.qmm_set_gemv_stream.restype = None
+        lib.qmm_gemv_stream_plan.argtypes = [ci, i64, i64, p]
         lib.qmm_quantize_q8_0.argtypes = [p, ci, i64, i64, p, p, p]
         lib.qmm_gemv_preq.argtypes = [ci, p, sz, i64, i64, p, p, i64, p, p]
         lib.qmm_q8act_workspace_bytes.argtypes = [i64, i64]
@@ -251,6 +254,21 @@ def qmm_set_gemv_tc(on: int) -> None:
     tensor-core kernel, 0 the ring kernel, -1 the environment's choice
     (QMM_GEMV_TC, default off)."""
     load().qmm_set_gemv_tc(int(on))
+
+
+def qmm_set_gemv_stream(rows_per_task: int, warps: int = 0, slots: int = 0, ctas_per_sm: int = 0) -> None:
+    """Plan parameters of the N = 1 streaming GEMV (see include/qmm.h):
+    0 = the planner's choice, -1 = the environment's."""
+    load().qmm_set_gemv_stream(int(rows_per_task), int(warps), int(slots), int(ctas_per_sm))
+
+
+def qmm_gemv_stream_plan(wt: int, M: int, K: int):
+    """(status, {grid, warps, slots, rows_per_task, smem}) of the streaming
+    GEMV for an M x K matrix under the present settings."""
+    out = (ctypes.c_int32 * 5)()
+    st = load().qmm_gemv_stream_plan(int(wt), int(M), int(K), out)
+    keys = ("grid", "warps", "slots", "rows_per_task", "smem")
+    return st, (dict(zip(keys, (int(v) for v in out))) if st == OK else None)
 
 
 def qmm_quantize_q8_0(X, N, K, scales, quants, stream=None, xt=None) -> int:
