@@ -828,20 +828,37 @@ bool plan_gemv_stream(int fmt, int64_t M, int64_t K, int num_sms, const StreamFo
     for (int attempt = 0; attempt < 8; ++attempt) {
         const int64_t rows = (M + grid - 1) / grid;
         const int64_t nst = ((rows + R - 1) / R * U + kLanes - 1) / kLanes;
-        // the most warps (at most 16 per SM) with one slot each: measured
-        // faster than fewer warps with 2 or 3 slots
+        // One slot per warp (measured faster than fewer warps with 2 or 3
+        // slots).  Warps: n_fit = the most that fit (at most 16 per SM); of
+        // the counts from 0.6 n_fit to n_fit, the one whose warps get the
+        // most even share of the CTA's stages -- a warp with one stage more
+        // than the others keeps the SM half idle at the end -- and among
+        // those the most warps.
         const int S = force.slots ? force.slots : 1;
-        for (int nw = force.warps ? force.warps : 16 / cps; nw >= 1; --nw) {
-            const StreamLayout L = stream_layout(fmt, R, nw, S, K, nst);
-            if (L.total <= lim) {
-                p.grid = (int)grid;
-                p.warps = nw;
-                p.S = S;
-                p.R = R;
-                p.smem = std::max(L.total, std::min(floor_smem, lim));
-                return true;
-            }
+        const double tasks = (double)((rows + R - 1) / R * U) / kLanes;   // stages, the last one fractional
+        int n_fit = 0;
+        for (int nw = force.warps ? force.warps : 16 / cps; nw >= 1 && !n_fit; --nw) {
+            if (stream_layout(fmt, R, nw, S, K, nst).total <= lim) n_fit = nw;
             if (force.warps) break;
+        }
+        int best = 0;
+        double best_bal = -1.0;
+        for (int nw = n_fit; nw >= 1 && 5 * nw >= 3 * n_fit && (!force.warps || nw == n_fit); --nw) {
+            const int64_t rounds = (nst + nw - 1) / nw;
+            const double bal = rounds <= 1 ? 1.0 : tasks / ((double)nw * rounds);
+            if (bal > best_bal + 0.02) {
+                best = nw;
+                best_bal = bal;
+            }
+        }
+        if (best) {
+            const StreamLayout L = stream_layout(fmt, R, best, S, K, nst);
+            p.grid = (int)grid;
+            p.warps = best;
+            p.S = S;
+            p.R = R;
+            p.smem = std::max(L.total, std::min(floor_smem, lim));
+            return true;
         }
         if (grid >= M) break;
         grid = grid * 2 < M ? grid * 2 : M;   // more, smaller CTAs: fewer partials each
