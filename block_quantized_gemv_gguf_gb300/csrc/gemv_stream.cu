@@ -813,8 +813,9 @@ bool plan_gemv_stream(int fmt, int64_t M, int64_t K, int num_sms, const StreamFo
         R = force.r;
     }
     // Two CTAs per SM for launches of short rows (K <= 4096: X is cheap to
-    // stage twice) up to 64 MB; one otherwise.
-    int cps = K <= 4096 && short_launch ? 2 : 1;
+    // stage twice) up to 64 MB with at least 8 rows per CTA; one otherwise
+    // (a launch of very few rows per SM is mostly the staging of X).
+    int cps = K <= 4096 && short_launch && M >= 16ll * num_sms ? 2 : 1;
     if (force.cps == 1 || force.cps == 2) cps = force.cps;
     if (force.warps > 16 / cps || force.slots > 3) return false;
     const int lim = cps == 2 ? kSmemPerSM / 2 - 3072 : kSmemMax;
@@ -843,7 +844,9 @@ bool plan_gemv_stream(int fmt, int64_t M, int64_t K, int num_sms, const StreamFo
         }
         int best = 0;
         double best_bal = -1.0;
-        for (int nw = n_fit; nw >= 1 && 5 * nw >= 3 * n_fit && (!force.warps || nw == n_fit); --nw) {
+        const bool one_round = !force.warps && n_fit > 8 && nst <= n_fit;
+        if (one_round) best = (int)std::max<int64_t>(8, nst);   // a warp per stage, at least 8
+        for (int nw = n_fit; !one_round && nw >= 1 && 5 * nw >= 3 * n_fit && (!force.warps || nw == n_fit); --nw) {
             const int64_t rounds = (nst + nw - 1) / nw;
             const double bal = rounds <= 1 ? 1.0 : tasks / ((double)nw * rounds);
             if (bal > best_bal + 0.02) {
