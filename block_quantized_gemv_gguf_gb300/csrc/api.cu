@@ -41,8 +41,9 @@ std::atomic<int> g_gemv_i8{-1};
 // through the API, take QMM_GEMV_TC from the environment (default off).
 std::atomic<int> g_gemv_tc{-1};
 // Streaming GEMV plan parameters set through qmm_set_gemv_stream (rows per
-// task, warps, slots, CTAs per SM): -1 = not set, take the environment's.
-std::atomic<int> g_stream_force[4] = {-1, -1, -1, -1};
+// task, warps, slots, CTAs per SM, direct-load variant): -1 = not set, take
+// the environment's.
+std::atomic<int> g_stream_force[5] = {-1, -1, -1, -1, -1};
 bool gemv_i8_on() {
     const int v = g_gemv_i8.load();
     if (v >= 0) return v != 0;
@@ -145,6 +146,7 @@ struct Settings {
     int stream_r;     // QMM_STREAM_R: rows per task of the streaming GEMV, 1, 2 or 4 (0 = by shape)
     int stream_slots; // QMM_STREAM_SLOTS: stage slots per warp, 1..3 (0 = by shared memory)
     int stream_cps;   // QMM_STREAM_CPS: CTAs per SM, 1 or 2 (0 = by shape)
+    int stream_direct;// QMM_STREAM_DIRECT: 1 the direct-load variant, 2 the staged kernel (0 = planner's choice)
     int tc;           // QMM_GEMV_TC: 1 enables the 16-row-tile tensor-core GEMV (opt-in, see qmm_set_gemv_tc)
     int tc_warps;     // QMM_TC_WARPS: warps per CTA of that kernel (0 = by shared memory)
     int tc_max_n;     // QMM_TC_MAX_N: largest N it serves (default 4; above, the ring GEMV is faster)
@@ -176,6 +178,8 @@ const Settings &settings() {
         if (t.stream_slots < 0 || t.stream_slots > 3) t.stream_slots = 0;
         t.stream_cps = env_int("QMM_STREAM_CPS", 0);
         if (t.stream_cps != 1 && t.stream_cps != 2) t.stream_cps = 0;
+        t.stream_direct = env_int("QMM_STREAM_DIRECT", 0);
+        if (t.stream_direct != 1 && t.stream_direct != 2) t.stream_direct = 0;
         t.tc = env_int("QMM_GEMV_TC", 0) != 0;
         t.tc_warps = env_int("QMM_TC_WARPS", 0);
         if (t.tc_warps != 4 && t.tc_warps != 8 && t.tc_warps != 16) t.tc_warps = 0;
@@ -189,13 +193,13 @@ const Settings &settings() {
 
 StreamForce stream_force() {
     const Settings &t = settings();
-    const int env[4] = {t.stream_r, t.stream_warps, t.stream_slots, t.stream_cps};
-    int v[4];
-    for (int i = 0; i < 4; ++i) {
+    const int env[5] = {t.stream_r, t.stream_warps, t.stream_slots, t.stream_cps, t.stream_direct};
+    int v[5];
+    for (int i = 0; i < 5; ++i) {
         const int g = g_stream_force[i].load();
         v[i] = g >= 0 ? g : env[i];
     }
-    return StreamForce{v[0], v[1], v[2], v[3]};
+    return StreamForce{v[0], v[1], v[2], v[3], v[4]};
 }
 
 // Common validation of W, M, K, X, N, Y.
@@ -724,9 +728,9 @@ void qmm_set_gemv_i8(int on) { g_gemv_i8.store(on < 0 ? -1 : (on ? 1 : 0)); }
 
 void qmm_set_gemv_tc(int on) { g_gemv_tc.store(on < 0 ? -1 : (on ? 1 : 0)); }
 
-void qmm_set_gemv_stream(int rows_per_task, int warps, int slots, int ctas_per_sm) {
-    const int v[4] = {rows_per_task, warps, slots, ctas_per_sm};
-    for (int i = 0; i < 4; ++i) g_stream_force[i].store(v[i] < 0 ? -1 : v[i]);
+void qmm_set_gemv_stream(int rows_per_task, int warps, int slots, int ctas_per_sm, int direct) {
+    const int v[5] = {rows_per_task, warps, slots, ctas_per_sm, direct};
+    for (int i = 0; i < 5; ++i) g_stream_force[i].store(v[i] < 0 ? -1 : v[i]);
 }
 
 qmm_status qmm_gemv_stream_plan(qmm_wtype wt, int64_t M, int64_t K, int32_t *plan) {
@@ -742,6 +746,7 @@ qmm_status qmm_gemv_stream_plan(qmm_wtype wt, int64_t M, int64_t K, int32_t *pla
     plan[2] = sp.S;
     plan[3] = sp.R;
     plan[4] = sp.smem;
+    plan[5] = sp.direct;
     return QMM_OK;
 }
 

@@ -707,6 +707,214 @@ __global__ void __launch_bounds__(512, 1) gemv_stream_kernel(const __grid_consta
     }
 }
 
+// ---------------------------------------------------------------------------
+// Direct-load variant for the 144-byte units (Q4_0, Q4_K): no shared-memory
+// ring and no mbarrier hand-off.  Each lane reads its own unit with nine
+// 16-byte read-only global loads straight into registers, two units per lane
+// in flight (ping-pong register buffers: the next unit's loads are issued
+// before the current unit's arithmetic).  X, the row reduction and the
+// partial sums are as in the staged kernel with one row per task.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void ldg_unit(uint32_t (&r)[36], const uint8_t *g) {
+    const uint4 *q = reinterpret_cast<const uint4 *>(g);
+#pragma unroll
+    for (int i = 0; i < 9; ++i) {
+        const uint4 v = __ldg(q + i);
+        r[4 * i] = v.x;
+        r[4 * i + 1] = v.y;
+        r[4 * i + 2] = v.z;
+        r[4 * i + 3] = v.w;
+    }
+}
+
+template <int F>
+__device__ __forceinline__ float unit_dot_regs(const uint32_t (&r)[36], const XRow &x, const float *xs8,
+                                               const float *fb8) {
+    float y = 0.f;
+    if constexpr (F == Q4_0) {
+        const float2 off = f2(-8388616.f, -8388616.f);   // -(2^23 + 8)
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            float2 acc = f2(0.f, 0.f);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const uint32_t w = word_at(r, 18 * b + 2 + 4 * t);
+                acc = dot4(acc, w & 0x0F0F0F0Fu, off, x(8 * b + t));
+                acc = dot4(acc, (w >> 4) & 0x0F0F0F0Fu, off, x(8 * b + 4 + t));
+            }
+            y = fmaf(f16_bits(half_at(r, 18 * b)), acc.x + acc.y, y);
+        }
+    } else {   // Q4_K
+        KHead hd;
+        hd.d = f16_bits(r[0] & 0xFFFFu);
+        hd.dmin = f16_bits(r[0] >> 16);
+        hd.scA = r[1] & 0x3F3F3F3Fu;
+        hd.mnA = r[2] & 0x3F3F3F3Fu;
+        hd.scB = (r[3] & 0x0F0F0F0Fu) | ((r[1] >> 2) & 0x30303030u);
+        hd.mnB = ((r[3] >> 4) & 0x0F0F0F0Fu) | ((r[2] >> 2) & 0x30303030u);
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            float2 alo = f2(0.f, 0.f), ahi = f2(0.f, 0.f);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                const uint32_t w = r[4 + 8 * p + t];
+                alo = dot4s(alo, w & 0x0F0F0F0Fu, x(16 * p + t));
+                ahi = dot4s(ahi, (w >> 4) & 0x0F0F0F0Fu, x(16 * p + 8 + t));
+            }
+            float2 dsc, dmn;
+            hd.pair(p, dsc, dmn);
+            y = fmaf(dsc.x, unscale(alo.x + alo.y, fb8[2 * p]), y);
+            y = fmaf(-dmn.x, xs8[2 * p], y);
+            y = fmaf(dsc.y, unscale(ahi.x + ahi.y, fb8[2 * p + 1]), y);
+            y = fmaf(-dmn.y, xs8[2 * p + 1], y);
+        }
+    }
+    return y;
+}
+
+template <int F, bool XBF16>
+__global__ void __launch_bounds__(512, 1) gemv_direct_kernel(const __grid_constant__ StreamArgs a) {
+    extern __shared__ __align__(1024) uint8_t sm[];
+    constexpr int UB = UnitBytes<F>::B;
+    static_assert(UB == 144, "direct loads: 144-byte units");
+    const int nw = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int U = a.K >> 8;
+    const int64_t r0 = (int64_t)blockIdx.x * a.M / gridDim.x;
+    const int64_t r1 = (int64_t)(blockIdx.x + 1) * a.M / gridDim.x;
+    const int nrows = (int)(r1 - r0);
+    const int nunits = nrows * U;
+    const int nst = (nunits + kLanes - 1) / kLanes;
+    const uint8_t *wcta = a.W + r0 * (int64_t)U * UB;
+    float *xs = reinterpret_cast<float *>(sm + a.off_x);
+    float *xsum = reinterpret_cast<float *>(sm + a.off_xsum);
+    float *part = reinterpret_cast<float *>(sm + a.off_part);
+    pdl_launch_dependents();
+
+    const int my_nst = warp < nst ? (nst - 1 - warp) / nw + 1 : 0;
+    auto unit_of = [&](int j) { return (warp + nw * j) * kLanes + lane; };
+    uint32_t ra[36], rb[36];
+    // the first two units: the weights do not depend on the preceding grid
+    if (my_nst > 0 && unit_of(0) < nunits) ldg_unit(ra, wcta + (int64_t)unit_of(0) * UB);
+    if (my_nst > 1 && unit_of(1) < nunits) ldg_unit(rb, wcta + (int64_t)unit_of(1) * UB);
+
+    pdl_wait();   // X and Y are ordered behind the preceding grid
+    {   // X -> shared memory, as in the staged kernel
+        float4 *xs4 = reinterpret_cast<float4 *>(xs);
+        const int nch = a.K >> 2;
+        constexpr int XB = 8;
+        for (int c0 = threadIdx.x; c0 < nch; c0 += XB * blockDim.x) {
+            float4 vb[XB];
+#pragma unroll
+            for (int i = 0; i < XB; ++i) {
+                const int c = c0 + i * (int)blockDim.x;
+                if (c < nch) {
+                    if constexpr (XBF16) {
+                        const uint2 b = reinterpret_cast<const uint2 *>(a.X)[c];
+                        vb[i] = make_float4(__uint_as_float(b.x << 16), __uint_as_float(b.x & 0xFFFF0000u),
+                                            __uint_as_float(b.y << 16), __uint_as_float(b.y & 0xFFFF0000u));
+                    } else {
+                        vb[i] = reinterpret_cast<const float4 *>(a.X)[c];
+                    }
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < XB; ++i) {
+                const int c = c0 + i * (int)blockDim.x;
+                if (c >= nch) break;
+                float4 v = vb[i];
+                if constexpr (kmin_fmt(F)) {
+                    float m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+                    float sx = (v.x + v.y) + (v.z + v.w);
+#pragma unroll
+                    for (int o = 1; o < 8; o <<= 1) {
+                        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                        sx += __shfl_xor_sync(0xffffffffu, sx, o);
+                    }
+                    int k = 126 - ((int)(__float_as_uint(m) >> 23) - 127);
+                    k = k < -1 ? -1 : (k > 127 ? 127 : k);
+                    const float sc = __uint_as_float((uint32_t)(127 + k) << 23);
+                    v.x *= sc;
+                    v.y *= sc;
+                    v.z *= sc;
+                    v.w *= sc;
+                    if ((c & 7) == 0) {
+                        xsum[c >> 3] = sx;
+                        xsum[(a.K >> 5) + (c >> 3)] = __uint_as_float((uint32_t)(212 - k) << 23);
+                    }
+                }
+                const int p = c >> 6, q = c & 63;
+                xs4[(p << 6) | (q ^ (p & 7))] = v;
+            }
+        }
+    }
+    __syncthreads();
+
+    const float4 *xs4 = reinterpret_cast<const float4 *>(xs);
+    float *__restrict__ Yc = a.Y + r0;
+    const bool amax = a.amax.keys != nullptr;
+    unsigned long long best = 0ull;
+    auto process = [&](int j, const uint32_t(&r)[36]) {
+        const int s = warp + nw * j;
+        const int u = s * kLanes + lane;
+        float v = 0.f;
+        int key = 0x7FFFFFFF;
+        if (u < nunits) {
+            key = u / U;
+            const int p = u - key * U;
+            v = unit_dot_regs<F>(r, XRow(xs4 + (p << 6), p & 7), xsum + 8 * p, xsum + (a.K >> 5) + 8 * p);
+        }
+#pragma unroll
+        for (int o = 1; o < kLanes; o <<= 1) {
+            const float vo = __shfl_down_sync(0xffffffffu, v, o);
+            const int ko = __shfl_down_sync(0xffffffffu, key, o);
+            if (lane + o < kLanes && ko == key) v += vo;
+        }
+        const int kp = __shfl_up_sync(0xffffffffu, key, 1);
+        if (u < nunits && (lane == 0 || kp != key)) {
+            const bool starts = key * U >= s * kLanes;
+            const bool ends = key * U + U <= (s + 1) * kLanes;
+            if (starts && ends) {
+                if (amax)
+                    amax_fold(best, v, (int)(r0 + key));
+                else
+                    Yc[key] = v;
+            } else
+                part[2 * s + (starts ? 1 : 0)] = v;
+        }
+    };
+    for (int j = 0; j < my_nst; j += 2) {
+        process(j, ra);
+        if (j + 2 < my_nst && unit_of(j + 2) < nunits) ldg_unit(ra, wcta + (int64_t)unit_of(j + 2) * UB);
+        if (j + 1 < my_nst) {
+            process(j + 1, rb);
+            if (j + 3 < my_nst && unit_of(j + 3) < nunits) ldg_unit(rb, wcta + (int64_t)unit_of(j + 3) * UB);
+        }
+    }
+    __syncthreads();
+    for (int rl = threadIdx.x; rl < nrows; rl += blockDim.x) {
+        const int sa = (rl * U) / kLanes, sb = (rl * U + U - 1) / kLanes;
+        if (sa == sb) continue;
+        float v = part[2 * sa + 1];
+        for (int s = sa + 1; s <= sb; ++s) v += part[2 * s];
+        if (amax)
+            amax_fold(best, v, (int)(r0 + rl));
+        else
+            Yc[rl] = v;
+    }
+    if (amax) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const unsigned long long x = __shfl_xor_sync(0xffffffffu, best, o);
+            best = x > best ? x : best;
+        }
+        if (lane == 0 && best != 0ull) {
+            atomicMax(a.amax.keys, best);
+            __threadfence();
+        }
+        amax_last_cta(a.amax, 1);
+    }
+}
+
 int unit_bytes_of(int fmt) {
     switch (fmt) {
     case Q8_0: return UnitBytes<Q8_0>::B;
@@ -745,9 +953,11 @@ StreamLayout stream_layout(int fmt, int R, int nw, int S, int64_t K, int64_t nst
     return L;
 }
 
-template <int F, bool XBF16, int R>
-cudaError_t launch_typed(const StreamPlan &p, const StreamArgs &a, bool pdl, cudaStream_t st) {
-    auto kern = gemv_stream_kernel<F, XBF16, R>;
+// Kern: the kernel itself (a template argument, so that each kernel keeps
+// its own record of the shared-memory attribute set on each device).
+template <auto Kern>
+cudaError_t launch_kernel(const StreamPlan &p, const StreamArgs &a, bool pdl, cudaStream_t st) {
+    const auto kern = Kern;
     static std::atomic<int> configured[64];   // largest dynamic shared memory set, per device
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -772,8 +982,16 @@ cudaError_t launch_typed(const StreamPlan &p, const StreamArgs &a, bool pdl, cud
     return launched(cudaGetLastError());
 }
 
+template <int F, bool XBF16, int R>
+cudaError_t launch_typed(const StreamPlan &p, const StreamArgs &a, bool pdl, cudaStream_t st) {
+    return launch_kernel<gemv_stream_kernel<F, XBF16, R>>(p, a, pdl, st);
+}
+
 template <int F, bool XBF16>
 cudaError_t launch_rows(const StreamPlan &p, const StreamArgs &a, bool pdl, cudaStream_t st) {
+    if constexpr (UnitBytes<F>::B == 144) {
+        if (p.direct) return launch_kernel<gemv_direct_kernel<F, XBF16>>(p, a, pdl, st);
+    }
     switch (p.R) {
     case 1: return launch_typed<F, XBF16, 1>(p, a, pdl, st);
     case 2: return launch_typed<F, XBF16, 2>(p, a, pdl, st);
@@ -812,6 +1030,9 @@ bool plan_gemv_stream(int fmt, int64_t M, int64_t K, int num_sms, const StreamFo
         if (!stage_contiguous(force.r, U) && ub % 16) return false;
         R = force.r;
     }
+    // The direct-load variant (144-byte units, one row per task): on request.
+    const bool direct = force.direct == 1 && ub == 144;
+    if (direct) R = 1;
     // Two CTAs per SM for launches of short rows (K <= 4096: X is cheap to
     // stage twice) up to 64 MB with at least 8 rows per CTA; one otherwise
     // (a launch of very few rows per SM is mostly the staging of X).
@@ -835,7 +1056,7 @@ bool plan_gemv_stream(int fmt, int64_t M, int64_t K, int num_sms, const StreamFo
         // most even share of the CTA's stages -- a warp with one stage more
         // than the others keeps the SM half idle at the end -- and among
         // those the most warps.
-        const int S = force.slots ? force.slots : 1;
+        const int S = direct ? 0 : force.slots ? force.slots : 1;
         const double tasks = (double)((rows + R - 1) / R * U) / kLanes;   // stages, the last one fractional
         int n_fit = 0;
         for (int nw = force.warps ? force.warps : 16 / cps; nw >= 1 && !n_fit; --nw) {
@@ -861,6 +1082,7 @@ bool plan_gemv_stream(int fmt, int64_t M, int64_t K, int num_sms, const StreamFo
             p.S = S;
             p.R = R;
             p.smem = std::max(L.total, std::min(floor_smem, lim));
+            p.direct = direct ? 1 : 0;
             return true;
         }
         if (grid >= M) break;

@@ -72,10 +72,12 @@ struct StreamPlan {
     int S;
     int R;      // rows per task: 1, 2 or 4
     int smem;   // dynamic shared memory bytes
+    int direct; // 1: the direct-load variant (registers, no shared-memory ring; S = 0)
 };
-// Requested plan parameters; 0 = chosen by the planner.  cps: CTAs per SM.
+// Requested plan parameters; 0 = chosen by the planner.  cps: CTAs per SM;
+// direct: 1 the direct-load variant, 2 the staged kernel.
 struct StreamForce {
-    int r, warps, slots, cps;
+    int r, warps, slots, cps, direct;
 };
 // false: the shape does not fit the kernel (another GEMV kernel runs), or
 // a forced parameter cannot be met.

@@ -78,7 +78,7 @@ def load() -> ctypes.CDLL:
         lib.qmm_set_gemv_i8.restype = None
         lib.qmm_set_gemv_tc.argtypes = [ctypes.c_int]
         lib.qmm_set_gemv_tc.restype = None
-        lib.qmm_set_gemv_stream.argtypes = [ci, ci, ci, ci]
+        lib.qmm_set_gemv_stream.argtypes = [ci, ci, ci, ci, ci]
         lib.qmm_set_gemv_stream.restype = None
         lib.qmm_gemv_stream_plan.argtypes = [ci, i64, i64, p]
         lib.qmm_quantize_q8_0.argtypes = [p, ci, i64, i64, p, p, p]
@@ -256,18 +256,19 @@ def qmm_set_gemv_tc(on: int) -> None:
     load().qmm_set_gemv_tc(int(on))
 
 
-def qmm_set_gemv_stream(rows_per_task: int, warps: int = 0, slots: int = 0, ctas_per_sm: int = 0) -> None:
+def qmm_set_gemv_stream(rows_per_task: int, warps: int = 0, slots: int = 0, ctas_per_sm: int = 0,
+                        direct: int = -1) -> None:
     """Plan parameters of the N = 1 streaming GEMV (see include/qmm.h):
     0 = the planner's choice, -1 = the environment's."""
-    load().qmm_set_gemv_stream(int(rows_per_task), int(warps), int(slots), int(ctas_per_sm))
+    load().qmm_set_gemv_stream(int(rows_per_task), int(warps), int(slots), int(ctas_per_sm), int(direct))
 
 
 def qmm_gemv_stream_plan(wt: int, M: int, K: int):
-    """(status, {grid, warps, slots, rows_per_task, smem}) of the streaming
+    """(status, {grid, warps, slots, rows_per_task, smem, direct}) of the streaming
     GEMV for an M x K matrix under the present settings."""
-    out = (ctypes.c_int32 * 5)()
+    out = (ctypes.c_int32 * 6)()
     st = load().qmm_gemv_stream_plan(int(wt), int(M), int(K), out)
-    keys = ("grid", "warps", "slots", "rows_per_task", "smem")
+    keys = ("grid", "warps", "slots", "rows_per_task", "smem", "direct")
     return st, (dict(zip(keys, (int(v) for v in out))) if st == OK else None)
 
 

@@ -352,25 +352,29 @@ QMM_API void qmm_set_gemv_tc(int on);
  * Plan of the one-token (N = 1) streaming GEMV, for tuning and tests.
  * rows_per_task: 1, 2 or 4 rows whose units at one 256-weight column one
  * lane computes against the same x values; warps: warps per CTA (1..16);
- * slots: stage slots per warp (1..3); ctas_per_sm: 1 or 2.  0 lets the
+ * slots: stage slots per warp (1..3); ctas_per_sm: 1 or 2; direct: 1 runs
+ * the direct-load variant where it applies (Q4_0 and Q4_K rows: each lane
+ * reads its unit with 16-byte global loads into registers, no shared-memory
+ * ring; one row per task, no slots), 2 the staged kernel.  0 lets the
  * planner choose that parameter; -1 returns it to the environment
- * (QMM_STREAM_R, QMM_STREAM_WARPS, QMM_STREAM_SLOTS, QMM_STREAM_CPS, each
- * 0 or unset for the planner's choice).  A shape whose forced plan does
- * not fit (shared memory, or rows per task above 1 for Q6_K rows whose
- * unit count does not divide 32) runs another GEMV kernel.  Every plan
- * computes the same per-unit sums in the same order; only the order in
- * which a row's unit sums are added can differ between plans.
- * Process-wide; takes effect at the next call.  The cera pages have no
- * counterpart: this is a GB300 kernel choice.
+ * (QMM_STREAM_R, QMM_STREAM_WARPS, QMM_STREAM_SLOTS, QMM_STREAM_CPS,
+ * QMM_STREAM_DIRECT, each 0 or unset for the planner's choice).  A shape
+ * whose forced plan does not fit (shared memory, or rows per task above 1
+ * for Q6_K rows whose unit count does not divide 32) runs another GEMV
+ * kernel.  Every plan computes the same per-unit sums; only the order in
+ * which a row's unit sums are added (and, for Q6_K, its sub-block sums)
+ * can differ between plans.  Process-wide; takes effect at the next call.
+ * The cera pages have no counterpart: this is a GB300 kernel choice.
  */
-QMM_API void qmm_set_gemv_stream(int rows_per_task, int warps, int slots, int ctas_per_sm);
+QMM_API void qmm_set_gemv_stream(int rows_per_task, int warps, int slots, int ctas_per_sm, int direct);
 
 /*
  * The streaming GEMV's plan for an M x K matrix of type wt on the current
- * device under the present settings: plan[0..4] = grid (CTAs), warps per
- * CTA, slots per warp, rows per task, dynamic shared memory bytes.  plan:
- * 5 host int32, caller-owned.  QMM_ERR_UNSUPPORTED: the shape does not fit
- * the kernel (qmm_gemv then runs another kernel); QMM_ERR_CUDA: no device.
+ * device under the present settings: plan[0..5] = grid (CTAs), warps per
+ * CTA, slots per warp, rows per task, dynamic shared memory bytes, 1 for
+ * the direct-load variant.  plan: 6 host int32, caller-owned.
+ * QMM_ERR_UNSUPPORTED: the shape does not fit the kernel (qmm_gemv then
+ * runs another kernel); QMM_ERR_CUDA: no device.
  */
 QMM_API qmm_status qmm_gemv_stream_plan(qmm_wtype wt, int64_t M, int64_t K, int32_t *plan);
 

@@ -41,7 +41,7 @@ def _lib():
         pytest.skip("needs a GPU")
     qmm.load()
     yield
-    qmm.qmm_set_gemv_stream(-1, -1, -1, -1)
+    qmm.qmm_set_gemv_stream(-1, -1, -1, -1, -1)
     torch.cuda.synchronize()
     assert qmm.qmm_last_device_error() == qmm.OK
 
@@ -51,10 +51,11 @@ def _aligned(wt, K):
     return (K // E * B) % 16 == 0
 
 
-def _run_plan(wt, plan):
-    """Returns the number of shapes the forced plan served."""
+def _run_plan(wt, plan, direct=2):
+    """Returns the number of shapes the forced plan served (direct: 2 the
+    staged kernel, 1 the direct-load variant)."""
     r, nw, s, cps = plan
-    qmm.qmm_set_gemv_stream(r, nw, s, cps)
+    qmm.qmm_set_gemv_stream(r, nw, s, cps, direct)
     served = 0
     try:
         for M, K in SHAPES:
@@ -66,7 +67,12 @@ def _run_plan(wt, plan):
                 # stage of 210-byte (Q6_K) units: another kernel would run
                 assert st == qmm.ERR_UNSUPPORTED
                 continue
-            assert p["rows_per_task"] == r and (nw == 0 or p["warps"] == nw) and (s == 0 or p["slots"] == s)
+            if direct == 1 and wt in (synth.Q4_0, synth.Q4_K):
+                assert p["direct"] == 1 and p["rows_per_task"] == 1 and p["slots"] == 0, p
+            else:
+                assert p["direct"] == 0, p
+                assert (r == 0 or p["rows_per_task"] == r) and (s == 0 or p["slots"] == s), p
+            assert nw == 0 or p["warps"] == nw, p
             w = synth.gen_weights(wt, M, K, f"rows-{M}-{K}")
             x = synth.gen_x(1, K, f"rows-{M}-{K}")
             W = torch.from_numpy(w).cuda()
@@ -86,7 +92,7 @@ def _run_plan(wt, plan):
             assert torch.equal(Y.view(torch.int32), Y2.view(torch.int32)), (M, K, "not deterministic")
             served += 1
     finally:
-        qmm.qmm_set_gemv_stream(-1, -1, -1, -1)
+        qmm.qmm_set_gemv_stream(-1, -1, -1, -1, -1)
     return served
 
 
@@ -100,6 +106,39 @@ def test_forced_plan_parity(wt, plan):
         assert served >= 1   # forced warps and slots fit only the smaller X / narrower units
 
 
+DIRECT_PLANS = [(0, 0, 0, 0), (0, 0, 0, 1), (0, 0, 0, 2), (0, 5, 0, 1), (0, 3, 0, 2)]
+
+
+@pytest.mark.parametrize("wt", ALL, ids=IDS)
+@pytest.mark.parametrize("plan", DIRECT_PLANS, ids=lambda p: "w{}-c{}".format(p[1], p[3]))
+def test_direct_variant_parity(wt, plan):
+    """The direct-load variant (Q4_0, Q4_K; other formats keep the staged
+    kernel when it is requested) on every shape and CTA shape."""
+    assert _run_plan(wt, plan, direct=1) >= 5   # two CTAs per SM cannot hold X of K = 28672
+
+
+@pytest.mark.parametrize("wt", [synth.Q4_0, synth.Q4_K], ids=["Q4_0", "Q4_K"])
+def test_direct_variant_argmax(wt):
+    M, K = 2999, 4096
+    w = synth.gen_weights(wt, M, K, "rows-amax")
+    x = synth.gen_x(1, K, "rows-amax")
+    W = torch.from_numpy(w).cuda()
+    X = torch.from_numpy(x).cuda()
+    qmm.qmm_set_gemv_stream(0, 0, 0, 0, 1)
+    try:
+        st, p = qmm.qmm_gemv_stream_plan(wt, M, K)
+        assert st == qmm.OK and p["direct"] == 1
+        idx, val = qmm.gemv_argmax(wt, W, M, K, X)
+        y = qmm.gemv(wt, W, M, K, X)
+        torch.cuda.synchronize()
+    finally:
+        qmm.qmm_set_gemv_stream(-1, -1, -1, -1, -1)
+    y = y.cpu().numpy()
+    j = int(np.argmax(y[0]))
+    assert int(idx.cpu()[0]) == j
+    assert val.cpu().numpy().view(np.uint32)[0] == y[0, j].view(np.uint32)
+
+
 @pytest.mark.parametrize("wt", [synth.Q4_0, synth.Q4_K, synth.Q6_K], ids=["Q4_0", "Q4_K", "Q6_K"])
 @pytest.mark.parametrize("r", [2, 4])
 def test_forced_plan_argmax(wt, r):
@@ -110,7 +149,7 @@ def test_forced_plan_argmax(wt, r):
     x = synth.gen_x(1, K, "rows-amax")
     W = torch.from_numpy(w).cuda()
     X = torch.from_numpy(x).cuda()
-    qmm.qmm_set_gemv_stream(r, 0, 0, 0)
+    qmm.qmm_set_gemv_stream(r, 0, 0, 0, 2)
     try:
         st, p = qmm.qmm_gemv_stream_plan(wt, M, K)
         assert st == qmm.OK and p["rows_per_task"] == r
@@ -118,7 +157,7 @@ def test_forced_plan_argmax(wt, r):
         y = qmm.gemv(wt, W, M, K, X)
         torch.cuda.synchronize()
     finally:
-        qmm.qmm_set_gemv_stream(-1, -1, -1, -1)
+        qmm.qmm_set_gemv_stream(-1, -1, -1, -1, -1)
     y = y.cpu().numpy()
     j = int(np.argmax(y[0]))
     assert int(idx.cpu()[0]) == j
