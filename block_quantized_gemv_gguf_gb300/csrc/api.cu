@@ -366,13 +366,22 @@ qmm_status gemv_segments(int wt, const SegIn *seg, int nseg, int64_t K, const vo
     if (q8) fast = fast && (uintptr_t)xscales % 16 == 0;
     // an explicit request for the integer kernel (N <= 2) takes precedence
     const bool want_i8 = !q8 && gemv_i8_on() && N <= 2;
-    if (fast && nseg == 1 && N == 1 && !q8 && !want_i8 && settings().stream) {
-        // one token: the streaming kernel, when the shape fits it
+    if (fast && N == 1 && !q8 && !want_i8 && settings().stream) {
+        // one token: the streaming kernel, when the shape fits it (several
+        // matrices sharing X run in the same launch)
+        const uint8_t *Ws[QMM_MAX_SEGS];
+        float *Ys[QMM_MAX_SEGS];
+        int64_t Ms[QMM_MAX_SEGS];
+        for (int i = 0; i < nseg; ++i) {
+            Ws[i] = static_cast<const uint8_t *>(seg[i].W);
+            Ys[i] = seg[i].Y;
+            Ms[i] = seg[i].M;
+        }
         StreamPlan sp{};
-        if (plan_gemv_stream(wt, seg[0].M, K, di.num_sms, stream_force(), sp))
-            return from_cuda(launch_gemv_stream(wt, sp, static_cast<const uint8_t *>(seg[0].W), seg[0].M, K, X,
-                                                xt == QMM_X_BF16, seg[0].Y, !amax && static_weights(), di.status,
-                                                g_wait_limit.load(), st, amax, idx, val));
+        if (plan_gemv_stream(wt, Ms, nseg, K, di.num_sms, stream_force(), sp))
+            return from_cuda(launch_gemv_stream(wt, sp, Ws, Ys, Ms, K, X, xt == QMM_X_BF16,
+                                                !amax && static_weights(), di.status, g_wait_limit.load(), st,
+                                                amax, idx, val));
     }
     const int tc_on = g_gemv_tc.load() >= 0 ? g_gemv_tc.load() : settings().tc;
     if (fast && nseg == 1 && N >= 2 && N <= settings().tc_max_n && !q8 && !want_i8 && tc_on &&

@@ -424,10 +424,14 @@ __device__ __forceinline__ void task_dot(const uint8_t *ub, int rs, const XRow &
 // The kernel.
 // ---------------------------------------------------------------------------
 struct StreamArgs {
-    const uint8_t *W;
+    // up to QMM_MAX_SEGS weight matrices sharing X: segment i has rows Ms[i]
+    // at Ws[i], output Ys[i], and CTAs cta0[i] .. cta0[i + 1] - 1
+    const uint8_t *Ws[QMM_MAX_SEGS];
+    float *Ys[QMM_MAX_SEGS];
+    int64_t Ms[QMM_MAX_SEGS];
+    int cta0[QMM_MAX_SEGS + 1];
+    int nseg;
     const void *X;
-    float *Y;
-    int64_t M;
     int K;
     int S;             // ring slots per warp
     int off_x;         // shared-memory offsets (bytes)
@@ -473,13 +477,16 @@ __global__ void __launch_bounds__(512, 1) gemv_stream_kernel(const __grid_consta
     const int nw = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int S = a.S;
     const int U = a.K >> 8;                                     // units per row
-    const int64_t r0 = (int64_t)blockIdx.x * a.M / gridDim.x;
-    const int64_t r1 = (int64_t)(blockIdx.x + 1) * a.M / gridDim.x;
+    int sg = 0;   // this CTA's weight matrix
+    while (sg + 1 < a.nseg && (int)blockIdx.x >= a.cta0[sg + 1]) ++sg;
+    const int lb = (int)blockIdx.x - a.cta0[sg], nb = a.cta0[sg + 1] - a.cta0[sg];
+    const int64_t r0 = (int64_t)lb * a.Ms[sg] / nb;
+    const int64_t r1 = (int64_t)(lb + 1) * a.Ms[sg] / nb;
     const int nrows = (int)(r1 - r0);
     const int ngrp = (nrows + R - 1) / R;                       // row groups (the last may be short)
     const int ntasks = ngrp * U;
     const int nst = (ntasks + kLanes - 1) / kLanes;            // stages of the CTA
-    const uint8_t *wcta = a.W + r0 * (int64_t)U * UB;
+    const uint8_t *wcta = a.Ws[sg] + r0 * (int64_t)U * UB;
     const bool contiguous = stage_contiguous(R, U);
 
     float *xs = reinterpret_cast<float *>(sm + a.off_x);
@@ -610,7 +617,7 @@ __global__ void __launch_bounds__(512, 1) gemv_stream_kernel(const __grid_consta
     __syncthreads();
 
     const float4 *xs4 = reinterpret_cast<const float4 *>(xs);
-    float *__restrict__ Yc = a.Y + r0;
+    float *__restrict__ Yc = a.Ys[sg] + r0;
     const bool amax = a.amax.keys != nullptr;
     unsigned long long best = 0ull;   // argmax mode: this thread's best (value, row) key
     int done = 0;   // stages of this warp consumed
@@ -779,12 +786,15 @@ __global__ void __launch_bounds__(512, 1) gemv_direct_kernel(const __grid_consta
     static_assert(UB == 144, "direct loads: 144-byte units");
     const int nw = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int U = a.K >> 8;
-    const int64_t r0 = (int64_t)blockIdx.x * a.M / gridDim.x;
-    const int64_t r1 = (int64_t)(blockIdx.x + 1) * a.M / gridDim.x;
+    int sg = 0;   // this CTA's weight matrix
+    while (sg + 1 < a.nseg && (int)blockIdx.x >= a.cta0[sg + 1]) ++sg;
+    const int lb = (int)blockIdx.x - a.cta0[sg], nb = a.cta0[sg + 1] - a.cta0[sg];
+    const int64_t r0 = (int64_t)lb * a.Ms[sg] / nb;
+    const int64_t r1 = (int64_t)(lb + 1) * a.Ms[sg] / nb;
     const int nrows = (int)(r1 - r0);
     const int nunits = nrows * U;
     const int nst = (nunits + kLanes - 1) / kLanes;
-    const uint8_t *wcta = a.W + r0 * (int64_t)U * UB;
+    const uint8_t *wcta = a.Ws[sg] + r0 * (int64_t)U * UB;
     float *xs = reinterpret_cast<float *>(sm + a.off_x);
     float *xsum = reinterpret_cast<float *>(sm + a.off_xsum);
     float *part = reinterpret_cast<float *>(sm + a.off_part);
@@ -850,7 +860,7 @@ __global__ void __launch_bounds__(512, 1) gemv_direct_kernel(const __grid_consta
     __syncthreads();
 
     const float4 *xs4 = reinterpret_cast<const float4 *>(xs);
-    float *__restrict__ Yc = a.Y + r0;
+    float *__restrict__ Yc = a.Ys[sg] + r0;
     const bool amax = a.amax.keys != nullptr;
     unsigned long long best = 0ull;
     auto process = [&](int j, const uint32_t(&r)[36]) {
@@ -1007,9 +1017,35 @@ cudaError_t launch_fmt(const StreamPlan &p, const StreamArgs &a, int xbf16, bool
 
 }  // namespace
 
+// Split `grid` CTAs over the segments in proportion to their rows (at least
+// one, at most M_i each); returns the most rows any CTA gets.
+static int64_t split_ctas(const int64_t *Ms, int nseg, int64_t M, int64_t grid, int (&cta0)[QMM_MAX_SEGS + 1]) {
+    int64_t rows_max = 0;
+    cta0[0] = 0;
+    for (int i = 0; i < nseg; ++i) {
+        int64_t c = (grid * Ms[i] + M / 2) / M;
+        c = c < 1 ? 1 : (c > Ms[i] ? Ms[i] : c);
+        cta0[i + 1] = cta0[i] + (int)c;
+        const int64_t r = (Ms[i] + c - 1) / c;
+        rows_max = r > rows_max ? r : rows_max;
+    }
+    return rows_max;
+}
+
 bool plan_gemv_stream(int fmt, int64_t M, int64_t K, int num_sms, const StreamForce &force, StreamPlan &p) {
+    return plan_gemv_stream(fmt, &M, 1, K, num_sms, force, p);
+}
+
+bool plan_gemv_stream(int fmt, const int64_t *Ms, int nseg, int64_t K, int num_sms, const StreamForce &force,
+                      StreamPlan &p) {
     const int ub = unit_bytes_of(fmt);
-    if (!ub || K % 256 || M < 1 || num_sms < 1 || K > (1 << 15)) return false;
+    if (nseg < 1 || nseg > QMM_MAX_SEGS) return false;
+    int64_t M = 0;   // all segments' rows
+    for (int i = 0; i < nseg; ++i) {
+        if (Ms[i] < 1) return false;
+        M += Ms[i];
+    }
+    if (!ub || K % 256 || num_sms < 1 || K > (1 << 15) || M > (1ll << 31) - 1) return false;
     if ((K / 256 * ub) % 16) return false;   // rows must start 16-byte aligned
     const int U = (int)(K / 256);
     const int64_t wbytes = M * U * ub;
@@ -1048,7 +1084,8 @@ bool plan_gemv_stream(int fmt, int64_t M, int64_t K, int num_sms, const StreamFo
     const int floor_smem = kSmemPerSM / (cps + 1) + 1024;
     int64_t grid = M < (int64_t)cps * num_sms ? M : (int64_t)cps * num_sms;
     for (int attempt = 0; attempt < 8; ++attempt) {
-        const int64_t rows = (M + grid - 1) / grid;
+        int cta0[QMM_MAX_SEGS + 1];
+        const int64_t rows = split_ctas(Ms, nseg, M, grid, cta0);
         const int64_t nst = ((rows + R - 1) / R * U + kLanes - 1) / kLanes;
         // One slot per warp (measured faster than fewer warps with 2 or 3
         // slots).  Warps: n_fit = the most that fit (at most 16 per SM); of
@@ -1077,7 +1114,9 @@ bool plan_gemv_stream(int fmt, int64_t M, int64_t K, int num_sms, const StreamFo
         }
         if (best) {
             const StreamLayout L = stream_layout(fmt, R, best, S, K, nst);
-            p.grid = (int)grid;
+            p.grid = cta0[nseg];
+            p.nseg = nseg;
+            for (int i = 0; i <= nseg; ++i) p.cta0[i] = cta0[i];
             p.warps = best;
             p.S = S;
             p.R = R;
@@ -1094,15 +1133,32 @@ bool plan_gemv_stream(int fmt, int64_t M, int64_t K, int num_sms, const StreamFo
 cudaError_t launch_gemv_stream(int fmt, const StreamPlan &p, const uint8_t *W, int64_t M, int64_t K, const void *X,
                                int xbf16, float *Y, bool pdl, unsigned *status, uint64_t limit, cudaStream_t st,
                                unsigned long long *amax_ws, int32_t *idx, float *val) {
-    const int64_t rows = (M + p.grid - 1) / p.grid;
+    return launch_gemv_stream(fmt, p, &W, &Y, &M, K, X, xbf16, pdl, status, limit, st, amax_ws, idx, val);
+}
+
+cudaError_t launch_gemv_stream(int fmt, const StreamPlan &p, const uint8_t *const *Ws, float *const *Ys,
+                               const int64_t *Ms, int64_t K, const void *X, int xbf16, bool pdl, unsigned *status,
+                               uint64_t limit, cudaStream_t st, unsigned long long *amax_ws, int32_t *idx,
+                               float *val) {
+    if (p.nseg < 1 || p.nseg > QMM_MAX_SEGS || (amax_ws && p.nseg != 1)) return cudaErrorInvalidValue;
+    StreamArgs a;
+    int64_t rows = 0;
+    for (int i = 0; i < p.nseg; ++i) {
+        const int c = p.cta0[i + 1] - p.cta0[i];
+        if (c < 1 || Ms[i] < 1) return cudaErrorInvalidValue;
+        const int64_t r = (Ms[i] + c - 1) / c;
+        rows = r > rows ? r : rows;
+        a.Ws[i] = Ws[i];
+        a.Ys[i] = Ys[i];
+        a.Ms[i] = Ms[i];
+    }
+    for (int i = 0; i <= p.nseg; ++i) a.cta0[i] = p.cta0[i];
+    a.nseg = p.nseg;
+    if (a.cta0[p.nseg] != p.grid) return cudaErrorInvalidValue;
     const int64_t nst = ((rows + p.R - 1) / p.R * (K / 256) + kLanes - 1) / kLanes;
     const StreamLayout L = stream_layout(fmt, p.R, p.warps, p.S, K, nst);
     if (L.total > p.smem) return cudaErrorInvalidValue;
-    StreamArgs a;
-    a.W = W;
     a.X = X;
-    a.Y = Y;
-    a.M = M;
     a.K = (int)K;
     a.S = p.S;
     a.off_x = L.off_x;

@@ -73,6 +73,8 @@ struct StreamPlan {
     int R;      // rows per task: 1, 2 or 4
     int smem;   // dynamic shared memory bytes
     int direct; // 1: the direct-load variant (registers, no shared-memory ring; S = 0)
+    int nseg;   // weight matrices sharing X; segment i runs on CTAs cta0[i] .. cta0[i + 1] - 1
+    int cta0[QMM_MAX_SEGS + 1];
 };
 // Requested plan parameters; 0 = chosen by the planner.  cps: CTAs per SM;
 // direct: 1 the direct-load variant, 2 the staged kernel.
@@ -82,12 +84,22 @@ struct StreamForce {
 // false: the shape does not fit the kernel (another GEMV kernel runs), or
 // a forced parameter cannot be met.
 bool plan_gemv_stream(int fmt, int64_t M, int64_t K, int num_sms, const StreamForce &force, StreamPlan &p);
+// The same for nseg (<= QMM_MAX_SEGS) matrices of Ms[i] rows sharing X and K:
+// one launch, the CTAs split over the matrices in proportion to their rows.
+bool plan_gemv_stream(int fmt, const int64_t *Ms, int nseg, int64_t K, int num_sms, const StreamForce &force,
+                      StreamPlan &p);
 // y[M] = W x.  pdl: programmatic dependent of the preceding kernel (the
 // weight copies start before it ends; X and Y wait for it).
 // amax_ws != nullptr: argmax mode as in launch_gemv_mma (Y is not written).
 cudaError_t launch_gemv_stream(int fmt, const StreamPlan &p, const uint8_t *W, int64_t M, int64_t K, const void *X,
                                int xbf16, float *Y, bool pdl, unsigned *status, uint64_t limit, cudaStream_t st,
                                unsigned long long *amax_ws = nullptr, int32_t *idx = nullptr, float *val = nullptr);
+// p.nseg matrices (Ws[i], Ms[i] rows, output Ys[i]) planned by the
+// multi-matrix plan_gemv_stream; argmax mode needs a single matrix.
+cudaError_t launch_gemv_stream(int fmt, const StreamPlan &p, const uint8_t *const *Ws, float *const *Ys,
+                               const int64_t *Ms, int64_t K, const void *X, int xbf16, bool pdl, unsigned *status,
+                               uint64_t limit, cudaStream_t st, unsigned long long *amax_ws = nullptr,
+                               int32_t *idx = nullptr, float *val = nullptr);
 
 // Tensor-core GEMV for 1 <= N <= 8 (mma.sync f16 on the exact codes) of
 // Q8_0 / Q4_0 / Q4_K / Q5_K rows (K % 256 == 0, K <= 32768, 16-byte aligned

@@ -120,3 +120,39 @@ def test_swiglu_errors():
     assert qmm.qmm_gemv_swiglu(wt, Wg, Wu, M, K, X, N, ws[:N * M].view(N, M), ws) == qmm.ERR_INVALID_ARG  # Y in ws
     assert qmm.qmm_gemv_swiglu(wt, Wg, Wu, M, K, X, 17, Y, ws) == qmm.ERR_INVALID_ARG
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("wt", [synth.Q8_0, synth.Q4_0, synth.Q4_K, synth.Q6_K, synth.Q5_K],
+                         ids=["Q8_0", "Q4_0", "Q4_K", "Q6_K", "Q5_K"])
+@pytest.mark.parametrize("plan", [(-1, -1, -1, -1, -1), (1, 0, 0, 1, 2), (2, 0, 0, 2, 2), (1, 0, 0, 0, 1)],
+                         ids=["auto", "r1-c1", "r2-c2", "direct"])
+def test_one_token_multi_streaming(wt, plan):
+    """N = 1 over several matrices runs the streaming kernel in one launch,
+    its CTAs split over the matrices by rows: four ragged matrices (1, 17,
+    300 and 4100 rows) and the Q/K/V shape, each plan."""
+    qmm.qmm_set_gemv_stream(*plan)
+    try:
+        _run(wt, [17, 4100, 1, 300], 2048, 1, f"ms-four-{wt}-{plan[0]}")
+        _run(wt, [4096, 1024, 1024], 4096, 1, f"ms-qkv-{wt}-{plan[0]}", xbf16=plan[0] == 2)
+    finally:
+        qmm.qmm_set_gemv_stream(-1, -1, -1, -1, -1)
+
+
+def test_one_token_multi_is_one_streaming_launch():
+    wt, K = synth.Q4_K, 4096
+    Ms = [4096, 1024, 1024]
+    Ws = [torch.from_numpy(synth.gen_weights(wt, M, K, f"ms1-{i}")).cuda() for i, M in enumerate(Ms)]
+    X = torch.from_numpy(synth.gen_x(1, K, "ms1")).cuda()
+    Ys = [torch.empty(1, M, device="cuda") for M in Ms]
+    torch.cuda.synchronize()
+    n0 = qmm.qmm_kernel_launches()
+    assert qmm.qmm_gemv_multi(wt, list(zip(Ws, Ms, Ys)), K, X, 1) == qmm.OK
+    torch.cuda.synchronize()
+    assert qmm.qmm_kernel_launches() - n0 == 1
+    from torch.profiler import ProfilerActivity, profile
+    with profile(activities=[ProfilerActivity.CUDA]) as prof:
+        assert qmm.qmm_gemv_multi(wt, list(zip(Ws, Ms, Ys)), K, X, 1) == qmm.OK
+        torch.cuda.synchronize()
+    names = [e.name for e in prof.events() if e.device_type == torch.autograd.DeviceType.CUDA]
+    if names:
+        assert any("gemv_stream_kernel" in n for n in names), names
