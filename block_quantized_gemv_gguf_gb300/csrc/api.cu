@@ -147,6 +147,7 @@ struct Settings {
     int stream_slots; // QMM_STREAM_SLOTS: stage slots per warp, 1..3 (0 = by shared memory)
     int stream_cps;   // QMM_STREAM_CPS: CTAs per SM, 1 or 2 (0 = by shape)
     int stream_direct;// QMM_STREAM_DIRECT: 1 the direct-load variant, 2 the staged kernel (0 = planner's choice)
+    int stream_stagger;// QMM_STREAM_STAGGER: 0 turns off the staggered stage issue of 2- and 3-slot plans
     int tc;           // QMM_GEMV_TC: 1 enables the 16-row-tile tensor-core GEMV (opt-in, see qmm_set_gemv_tc)
     int tc_warps;     // QMM_TC_WARPS: warps per CTA of that kernel (0 = by shared memory)
     int tc_max_n;     // QMM_TC_MAX_N: largest N it serves (default 4; above, the ring GEMV is faster)
@@ -180,6 +181,7 @@ const Settings &settings() {
         if (t.stream_cps != 1 && t.stream_cps != 2) t.stream_cps = 0;
         t.stream_direct = env_int("QMM_STREAM_DIRECT", 0);
         if (t.stream_direct != 1 && t.stream_direct != 2) t.stream_direct = 0;
+        t.stream_stagger = env_int("QMM_STREAM_STAGGER", 1) == 0 ? 2 : 0;
         t.tc = env_int("QMM_GEMV_TC", 0) != 0;
         t.tc_warps = env_int("QMM_TC_WARPS", 0);
         if (t.tc_warps != 4 && t.tc_warps != 8 && t.tc_warps != 16) t.tc_warps = 0;
@@ -199,7 +201,7 @@ StreamForce stream_force() {
         const int g = g_stream_force[i].load();
         v[i] = g >= 0 ? g : env[i];
     }
-    return StreamForce{v[0], v[1], v[2], v[3], v[4]};
+    return StreamForce{v[0], v[1], v[2], v[3], v[4], t.stream_stagger};
 }
 
 // Common validation of W, M, K, X, N, Y.

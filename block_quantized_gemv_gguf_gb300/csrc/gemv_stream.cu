@@ -434,6 +434,7 @@ struct StreamArgs {
     const void *X;
     int K;
     int S;             // ring slots per warp
+    int stagger;       // S >= 2: one stage issued up front, stage j + S - 1 once stage j has landed
     int off_x;         // shared-memory offsets (bytes)
     int off_xsum;
     int off_part;
@@ -553,7 +554,9 @@ __global__ void __launch_bounds__(512, 1) gemv_stream_kernel(const __grid_consta
         }
     };
     // weights first: they do not depend on the preceding grid
-    for (int j = 0; j < S && j < my_nst; ++j) issue(j);
+    const bool stagger = a.stagger && S >= 2;
+    int nissued = 0;   // stages of this warp issued so far (warp-uniform)
+    for (; nissued < (stagger ? 1 : S) && nissued < my_nst; ++nissued) issue(nissued);
 
     pdl_wait();   // X and Y are ordered behind the preceding grid
 
@@ -624,6 +627,9 @@ __global__ void __launch_bounds__(512, 1) gemv_stream_kernel(const __grid_consta
     for (int j = 0; j < my_nst; ++j) {
         const int slot = warp * S + j % S;
         if (!warp_wait(abort_flag, &bars[slot], (uint32_t)(j / S) & 1u, a.limit)) break;
+        // staggered: the next stage's copy goes out as soon as this one has
+        // landed (its slot held stage j - 1, consumed last iteration)
+        for (; stagger && nissued < my_nst && nissued <= j + S - 1; ++nissued) issue(nissued);
         const int s = warp + nw * j;
         const int t0 = s * kLanes;
         const int te = min(t0 + kLanes, ntasks);
@@ -643,7 +649,7 @@ __global__ void __launch_bounds__(512, 1) gemv_stream_kernel(const __grid_consta
             for (int i = 0; i < R; ++i) v[i] = 0.f;
         }
         __syncwarp();
-        if (j + S < my_nst) issue(j + S);   // every lane has read the slot
+        if (!stagger && j + S < my_nst) issue(nissued++);   // every lane has read the slot: stage j + S
         done = j + 1;
         // segmented reduction by row group: each group's first lane of the
         // stage ends up with the stage's sums for the group's rows
@@ -678,8 +684,7 @@ __global__ void __launch_bounds__(512, 1) gemv_stream_kernel(const __grid_consta
     }
     // copies still in flight (only after an abort): wait for them before exit
     if (lane == 0) {
-        const int issued = my_nst < done + S ? my_nst : done + S;
-        for (int j = done; j < issued; ++j)
+        for (int j = done; j < nissued; ++j)
             (void)mbar_wait(&bars[warp * S + j % S], (uint32_t)(j / S) & 1u,
                             a.limit < (1ull << 31) ? (1ull << 31) : a.limit);
     }
@@ -1087,31 +1092,45 @@ bool plan_gemv_stream(int fmt, const int64_t *Ms, int nseg, int64_t K, int num_s
         int cta0[QMM_MAX_SEGS + 1];
         const int64_t rows = split_ctas(Ms, nseg, M, grid, cta0);
         const int64_t nst = ((rows + R - 1) / R * U + kLanes - 1) / kLanes;
-        // One slot per warp (measured faster than fewer warps with 2 or 3
-        // slots).  Warps: n_fit = the most that fit (at most 16 per SM); of
-        // the counts from 0.6 n_fit to n_fit, the one whose warps get the
-        // most even share of the CTA's stages -- a warp with one stage more
-        // than the others keeps the SM half idle at the end -- and among
-        // those the most warps.
-        const int S = direct ? 0 : force.slots ? force.slots : 1;
+        // Warps for S slots each: n_fit = the most that fit (at most 16 per
+        // SM); of the counts from 0.6 n_fit to n_fit, the one whose warps get
+        // the most even share of the CTA's stages -- a warp with one stage
+        // more than the others keeps the SM half idle at the end -- and among
+        // those the most warps; a warp per stage (at least 8) when one round
+        // covers the CTA.  Returns 0 if nothing fits.
         const double tasks = (double)((rows + R - 1) / R * U) / kLanes;   // stages, the last one fractional
-        int n_fit = 0;
-        for (int nw = force.warps ? force.warps : 16 / cps; nw >= 1 && !n_fit; --nw) {
-            if (stream_layout(fmt, R, nw, S, K, nst).total <= lim) n_fit = nw;
-            if (force.warps) break;
-        }
-        int best = 0;
-        double best_bal = -1.0;
-        const bool one_round = !force.warps && n_fit > 8 && nst <= n_fit;
-        if (one_round) best = (int)std::max<int64_t>(8, nst);   // a warp per stage, at least 8
-        for (int nw = n_fit; !one_round && nw >= 1 && 5 * nw >= 3 * n_fit && (!force.warps || nw == n_fit); --nw) {
-            const int64_t rounds = (nst + nw - 1) / nw;
-            const double bal = rounds <= 1 ? 1.0 : tasks / ((double)nw * rounds);
-            if (bal > best_bal + 0.02) {
-                best = nw;
-                best_bal = bal;
+        auto choose = [&](int S, int &n_fit, int64_t &rounds) {
+            n_fit = 0;
+            for (int nw = force.warps ? force.warps : 16 / cps; nw >= 1 && !n_fit; --nw) {
+                if (stream_layout(fmt, R, nw, S, K, nst).total <= lim) n_fit = nw;
+                if (force.warps) break;
             }
-        }
+            int best = 0;
+            double best_bal = -1.0;
+            const bool one_round = !force.warps && n_fit > 8 && nst <= n_fit;
+            if (one_round) best = (int)std::max<int64_t>(8, nst);
+            for (int nw = n_fit; !one_round && nw >= 1 && 5 * nw >= 3 * n_fit && (!force.warps || nw == n_fit);
+                 --nw) {
+                const int64_t r = (nst + nw - 1) / nw;
+                const double bal = r <= 1 ? 1.0 : tasks / ((double)nw * r);
+                if (bal > best_bal + 0.02) {
+                    best = nw;
+                    best_bal = bal;
+                }
+            }
+            rounds = best ? (nst + best - 1) / best : 0;
+            return best;
+        };
+        // Slots: one per warp unless forced.  Two slots with staggered issue
+        // (stage j + 1's copy goes out once stage j has landed) run the big
+        // shapes alone 3-4% faster (14336 x 4096, 4096 x 14336), but their
+        // larger footprint keeps the next launch's CTAs off the SM until
+        // they exit: the following launch lost as much, and a 32-layer
+        // decoder sequence ran 3% slower.
+        const int S = direct ? 0 : force.slots ? force.slots : 1;
+        int n_fit = 0;
+        int64_t rounds = 0;
+        const int best = choose(S, n_fit, rounds);
         if (best) {
             const StreamLayout L = stream_layout(fmt, R, best, S, K, nst);
             p.grid = cta0[nseg];
@@ -1122,6 +1141,7 @@ bool plan_gemv_stream(int fmt, const int64_t *Ms, int nseg, int64_t K, int num_s
             p.R = R;
             p.smem = std::max(L.total, std::min(floor_smem, lim));
             p.direct = direct ? 1 : 0;
+            p.stagger = S >= 2 && force.stagger != 2 ? 1 : 0;
             return true;
         }
         if (grid >= M) break;
@@ -1161,6 +1181,7 @@ cudaError_t launch_gemv_stream(int fmt, const StreamPlan &p, const uint8_t *cons
     a.X = X;
     a.K = (int)K;
     a.S = p.S;
+    a.stagger = p.stagger;
     a.off_x = L.off_x;
     a.off_xsum = L.off_xsum;
     a.off_part = L.off_part;

@@ -73,6 +73,7 @@ struct StreamPlan {
     int R;      // rows per task: 1, 2 or 4
     int smem;   // dynamic shared memory bytes
     int direct; // 1: the direct-load variant (registers, no shared-memory ring; S = 0)
+    int stagger;// S >= 2: one stage issued up front, the next once the current has landed
     int nseg;   // weight matrices sharing X; segment i runs on CTAs cta0[i] .. cta0[i + 1] - 1
     int cta0[QMM_MAX_SEGS + 1];
 };
@@ -80,6 +81,7 @@ struct StreamPlan {
 // direct: 1 the direct-load variant, 2 the staged kernel.
 struct StreamForce {
     int r, warps, slots, cps, direct;
+    int stagger;   // 2: no staggered stage issue with slots >= 2 (on otherwise)
 };
 // false: the shape does not fit the kernel (another GEMV kernel runs), or
 // a forced parameter cannot be met.

@@ -121,6 +121,9 @@ print("BAD" if bad else "OK", bad)
 
 @pytest.mark.parametrize("env", [{"QMM_STREAM_WARPS": "4"}, {"QMM_STREAM_WARPS": "8"},
                                  {"QMM_STREAM_WARPS": "12"}, {"QMM_STREAM_WARPS": "16"},
+                                 {"QMM_STREAM_SLOTS": "2"}, {"QMM_STREAM_SLOTS": "3"},
+                                 {"QMM_STREAM_SLOTS": "2", "QMM_STREAM_STAGGER": "0"},
+                                 {"QMM_STREAM_SLOTS": "3", "QMM_STREAM_STAGGER": "0"},
                                  {"QMM_GEMV_STREAM": "0"}, {"QMM_STATIC_WEIGHTS": "1"}],
                          ids=lambda e: "-".join(f"{k[4:].lower()}{v}" for k, v in e.items()))
 def test_stream_forced_shapes(env):
