@@ -4,22 +4,25 @@
 //
 // the per-token projection of "cera 0.5.0 src/model/llama.rs" (decode) and
 // the row loops of "cera 0.5.2 src/backend/cpu.rs" (matmul_*_f32 /
-// gemv_dispatch), restated for one GB300 SM per CTA:
+// gemv_dispatch), restated for GB300 SMs (one or two CTAs per SM):
 //
 //   * Unit = 256 consecutive weights of one row (8 Q4_0 / Q8_0 blocks, or
 //     one Q4_K / Q5_K / Q6_K super-block): 144, 272, 176 or 210 bytes.
-//     A CTA owns whole rows; its rows are one contiguous byte range of W.
-//   * Task = the units of R consecutive rows (a "row group") at one unit
-//     column p: the R units share the same 256 x values, which a lane reads
-//     from shared memory once and applies to all R rows.  With R = 4 the
+//     A CTA owns whole rows of one weight matrix; its rows are one
+//     contiguous byte range of W.  Up to four matrices sharing X and K run
+//     in one launch, the CTAs split over them by rows (a segment table).
+//   * Task = the units of R consecutive rows (a "row group", R = 1, 2 or 4)
+//     at one unit column p: the R units share the same 256 x values, which
+//     a lane reads from shared memory once and applies to all R rows, so the
 //     shared-memory traffic of X (4 bytes per weight at R = 1, against 0.56
-//     bytes of Q4_0 weights) drops four-fold.
+//     bytes of Q4_0 weights) drops R-fold.
 //   * Tasks are numbered group-major (t = g U + p, U units per row).  Each
 //     warp streams its own "stages" of 32 consecutive tasks: one bulk copy
 //     per (row, run of columns) piece of the stage -- a single copy when the
 //     stage is contiguous in W -- completing on a warp-private mbarrier, in a
-//     ring of S slots.  Lane l owns task l of the stage.  No data passes
-//     between warps until the very end.
+//     ring of S slots (S >= 2: each stage issued once the previous one has
+//     landed).  Lane l owns task l of the stage.  No data passes between
+//     warps until the very end.
 //   * The weight copies are issued before the kernel waits on the preceding
 //     grid (the weights are static; X and Y are ordered behind it).
 //   * X (f32; bf16 widened) sits in shared memory once per CTA, in 16-byte
@@ -27,13 +30,18 @@
 //     each on its own column, read it without bank conflicts.
 //   * Arithmetic: every integer code becomes an exact f32 by a byte permute
 //     into the mantissa of 2^23 and one packed subtraction (which also
-//     removes the format's offset), then a packed f32 FMA with x.  Each
-//     block's (or sub-block's) scale multiplies the f32 block sum; the
-//     Q4_K / Q5_K min term uses the sub-block sums of x.
+//     removes the format's offset), then a packed f32 FMA with x; Q4_K and
+//     Q5_K codes, which carry no offset, are exact f32 subnormals against X
+//     scaled per block by a power of two.  Each block's (or sub-block's)
+//     scale multiplies the f32 block sum; the Q4_K / Q5_K min term uses the
+//     sub-block sums of x.
 //   * Row results: a segmented warp-shuffle reduction by row group over each
 //     stage (a group held entirely in one stage is stored directly); groups
 //     that cross stages are summed from per-stage partials in stage order at
 //     the end.  Every sum has a fixed order: the result is deterministic.
+//   * plan_gemv_stream picks R, CTAs per SM, warps and slots from the shape
+//     (rules measured on GB300, stated there); gemv_direct_kernel, a variant
+//     that loads each lane's unit straight into registers, runs on request.
 //
 // All waits are bounded; a warp that gives up raises the CTA's abort flag,
 // waits (bounded) for its own copies in flight, and the CTA reports
@@ -1092,35 +1100,6 @@ bool plan_gemv_stream(int fmt, const int64_t *Ms, int nseg, int64_t K, int num_s
         int cta0[QMM_MAX_SEGS + 1];
         const int64_t rows = split_ctas(Ms, nseg, M, grid, cta0);
         const int64_t nst = ((rows + R - 1) / R * U + kLanes - 1) / kLanes;
-        // Warps for S slots each: n_fit = the most that fit (at most 16 per
-        // SM); of the counts from 0.6 n_fit to n_fit, the one whose warps get
-        // the most even share of the CTA's stages -- a warp with one stage
-        // more than the others keeps the SM half idle at the end -- and among
-        // those the most warps; a warp per stage (at least 8) when one round
-        // covers the CTA.  Returns 0 if nothing fits.
-        const double tasks = (double)((rows + R - 1) / R * U) / kLanes;   // stages, the last one fractional
-        auto choose = [&](int S, int &n_fit, int64_t &rounds) {
-            n_fit = 0;
-            for (int nw = force.warps ? force.warps : 16 / cps; nw >= 1 && !n_fit; --nw) {
-                if (stream_layout(fmt, R, nw, S, K, nst).total <= lim) n_fit = nw;
-                if (force.warps) break;
-            }
-            int best = 0;
-            double best_bal = -1.0;
-            const bool one_round = !force.warps && n_fit > 8 && nst <= n_fit;
-            if (one_round) best = (int)std::max<int64_t>(8, nst);
-            for (int nw = n_fit; !one_round && nw >= 1 && 5 * nw >= 3 * n_fit && (!force.warps || nw == n_fit);
-                 --nw) {
-                const int64_t r = (nst + nw - 1) / nw;
-                const double bal = r <= 1 ? 1.0 : tasks / ((double)nw * r);
-                if (bal > best_bal + 0.02) {
-                    best = nw;
-                    best_bal = bal;
-                }
-            }
-            rounds = best ? (nst + best - 1) / best : 0;
-            return best;
-        };
         // Slots: one per warp unless forced.  Two slots with staggered issue
         // (stage j + 1's copy goes out once stage j has landed) run the big
         // shapes alone 3-4% faster (14336 x 4096, 4096 x 14336), but their
@@ -1128,9 +1107,29 @@ bool plan_gemv_stream(int fmt, const int64_t *Ms, int nseg, int64_t K, int num_s
         // they exit: the following launch lost as much, and a 32-layer
         // decoder sequence ran 3% slower.
         const int S = direct ? 0 : force.slots ? force.slots : 1;
+        // Warps: n_fit = the most that fit (at most 16 per SM); of the counts
+        // from 0.6 n_fit to n_fit, the one whose warps get the most even share
+        // of the CTA's stages -- a warp with one stage more than the others
+        // keeps the SM half idle at the end -- and among those the most
+        // warps; a warp per stage (at least 8) when one round covers the CTA.
+        const double tasks = (double)((rows + R - 1) / R * U) / kLanes;   // stages, the last one fractional
         int n_fit = 0;
-        int64_t rounds = 0;
-        const int best = choose(S, n_fit, rounds);
+        for (int nw = force.warps ? force.warps : 16 / cps; nw >= 1 && !n_fit; --nw) {
+            if (stream_layout(fmt, R, nw, S, K, nst).total <= lim) n_fit = nw;
+            if (force.warps) break;
+        }
+        int best = 0;
+        double best_bal = -1.0;
+        const bool one_round = !force.warps && n_fit > 8 && nst <= n_fit;
+        if (one_round) best = (int)std::max<int64_t>(8, nst);
+        for (int nw = n_fit; !one_round && nw >= 1 && 5 * nw >= 3 * n_fit && (!force.warps || nw == n_fit); --nw) {
+            const int64_t r = (nst + nw - 1) / nw;
+            const double bal = r <= 1 ? 1.0 : tasks / ((double)nw * r);
+            if (bal > best_bal + 0.02) {
+                best = nw;
+                best_bal = bal;
+            }
+        }
         if (best) {
             const StreamLayout L = stream_layout(fmt, R, best, S, K, nst);
             p.grid = cta0[nseg];
