@@ -76,11 +76,11 @@ def peaks():
 # sha256 of the kernel sources they were taken on: any source change since
 # the capture turns the figure into null.
 TRAFFIC = {
-    # kernel sources ee75fbdfc50905b4: the launch list of `bench.py --steps 8 --copies 2 --no-extras` under ncu
-    "decode": ("ee75fbdfc50905b4", 78_154_000),       # 4 launches of the streaming GEMV
-    "lmhead": ("ee75fbdfc50905b4", 452_247_000),      # ring GEMV, Q6_K 128256x4096, N=8
-    "prefill": ("ee75fbdfc50905b4", 55_148_000),      # 3 GEMM launches (bf16 X)
-    "prefill_f32": ("ee75fbdfc50905b4", 71_958_000),  # 2 conversions + 3 GEMM launches
+    # kernel sources 865a33c78cf96faa: the launch list of `bench.py --steps 8 --copies 2 --no-extras` under ncu
+    "decode": ("865a33c78cf96faa", 78_156_000),       # 4 launches of the streaming GEMV
+    "lmhead": ("865a33c78cf96faa", 452_213_000),      # ring GEMV, Q6_K 128256x4096, N=8
+    "prefill": ("865a33c78cf96faa", 55_158_000),      # 3 GEMM launches (bf16 X)
+    "prefill_f32": ("865a33c78cf96faa", 71_933_000),  # 2 conversions + 3 GEMM launches
 }
 
 
